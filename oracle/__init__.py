@@ -1,0 +1,14 @@
+"""Float64 CPU oracle of the Mamba-2 SSD layer -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA library
+and imports nothing from it.
+
+  ssd_ref      -- ctypes wrapper over ``ssd_oracle.c``: the sequential
+                  recurrence (forward) and its hand-derived reverse mode.
+  chunked      -- numpy float64 evaluation of the same layer by chunks
+                  (chunk states, state passing, intra-chunk output), forward
+                  and backward, returning the intermediates as well.
+  scan         -- the pair-combine operator of the associative scan and a
+                  Hillis-Steele log-step scan built on it.
+"""
