@@ -1,0 +1,141 @@
+/*
+ * ssd.h -- C ABI of libssd: the Mamba-2 selective state-space (SSD) layer's
+ * chunked scan, forward and backward, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (page "llm-mamba-200" (gigipick.blogspot.com), sections 1-2:
+ * a selective linear recurrence whose steps combine associatively; the
+ * equations are lost from the page text and are taken in their Mamba-2 form
+ * with one scalar decay per head):
+ *
+ *   dt_eff[t,h] = softplus(dt[t,h] + dt_bias[h])
+ *   h_t         = exp(dt_eff[t,h] * A[h]) * h_{t-1} + dt_eff[t,h] * x_t (outer) B_t
+ *   y_t         = h_t . C_t + D[h] * x_t
+ *
+ * per batch row and head, with h_{-1} = initial_states (or 0).  When seq_idx
+ * is given, a token whose id differs from the previous token's starts a new
+ * sequence with a zero state; initial_states feeds only the first one.
+ * final_states is the state after the last token.
+ *
+ * It is evaluated by chunks of chunk_size tokens (page "llm-mamba-200",
+ * section 3: carry-out state of one chunk is the carry-in of the next), with
+ * the cross-chunk state passing, forward and backward, done as an associative
+ * scan (page "B200 Helion Mamba-2" (aitrends.kr/articles/109906), section
+ * "Helion based B200 kernel redesign").
+ *
+ * Shapes (b = batch, L = seqlen, H = nheads, P = headdim, N = dstate,
+ * G = ngroups; head h reads group floor(h*G/H), i.e. G contiguous blocks of
+ * H/G heads).  Every tensor is dense row-major, device memory:
+ *
+ *   x, y, dy, dx            (b, L, H, P)   dtype
+ *   dt, ddt                 (b, L, H)      dtype
+ *   B, C, dB, dC            (b, L, G, N)   dtype
+ *   dt_bias, A, D and grads (H)            fp32
+ *   initial_states, final_states, dfinal_states, dinitial_states
+ *                           (b, H, P, N)   fp32
+ *   seq_idx                 (b, L)         int32, nondecreasing along each row
+ *
+ * where dtype is SSD_F32 (fp32) or SSD_BF16 (bf16; fp32 accumulation inside).
+ * Every pointer must be 16-byte aligned.
+ *
+ * Ownership: the caller allocates every buffer, the workspace included, and
+ * keeps them alive until the stream work completes.  The library never
+ * allocates, never synchronises (except ssd_read_device_status) and keeps no
+ * mutable global state other than a per-device cache of device attributes.
+ * Calls enqueue work on the given stream and return before it completes.
+ *
+ * Errors: every entry point validates its arguments before enqueuing
+ * anything and returns an ssd_status; nothing is thrown across the ABI.
+ * Errors detected on the device (a bounded wait that expired) are recorded
+ * in a status word at the start of the workspace; read it with
+ * ssd_read_device_status.
+ */
+#ifndef SSD_H_
+#define SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ssd_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARGUMENT = 1, /* null required pointer, bad dims, misaligned pointer */
+  SSD_ERR_UNSUPPORTED = 2,      /* shape/dtype outside the compiled set, or not an sm_103 device */
+  SSD_ERR_WORKSPACE_TOO_SMALL = 3,
+  SSD_ERR_CUDA = 4,             /* a CUDA runtime error while enqueuing */
+  SSD_ERR_TIMEOUT = 5           /* a device-side bounded wait expired (read via the status word) */
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+enum {
+  SSD_HAS_INIT = 1,      /* initial_states is given */
+  SSD_HAS_SEQ_IDX = 2,   /* seq_idx is given */
+  SSD_HAS_DFINAL = 4,    /* ssd_bwd: dfinal_states (upstream gradient of final_states) is given */
+  SSD_WANT_DINIT = 8,    /* ssd_bwd: write dinitial_states */
+  /* Testing only: the first scan tile of the first state chain never
+   * publishes its prefix, so the tiles after it exhaust their bounded wait
+   * (0.1 s with this flag, 2 s otherwise) and the call ends with
+   * SSD_ERR_TIMEOUT in the device status word instead of hanging.  Results
+   * of such a call are garbage. */
+  SSD_TEST_DROP_SCAN_PUBLISH = 1 << 16
+};
+
+typedef struct {
+  int64_t batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size;
+  int32_t dtype; /* ssd_dtype */
+  int32_t flags; /* SSD_HAS_* / SSD_WANT_* */
+} ssd_problem;
+
+/* Limits of the compiled kernels (checked by every entry point):
+ *   1 <= chunk_size <= 256, chunk_size % 16 == 0
+ *   headdim in {16, 32, 64, 128}; dstate in {16, 32, 64, 128};
+ *   headdim * dstate <= 8192
+ *   nheads % ngroups == 0; batch, seqlen >= 1                              */
+
+/* Bytes of device workspace ssd_fwd / ssd_bwd need for this problem
+ * (a pure function of the problem; 0 if the problem is invalid). */
+size_t ssd_fwd_workspace_bytes(const ssd_problem* prob);
+size_t ssd_bwd_workspace_bytes(const ssd_problem* prob);
+
+/* Forward.  Writes y and (if non-NULL) final_states.  initial_states must be
+ * non-NULL iff SSD_HAS_INIT, seq_idx iff SSD_HAS_SEQ_IDX.  Enqueues on
+ * `stream` and returns without waiting. */
+int ssd_fwd(const ssd_problem* prob, const void* x, const void* dt, const float* dt_bias,
+            const float* A, const void* B, const void* C, const float* D,
+            const float* initial_states, const int32_t* seq_idx, void* y, float* final_states,
+            void* workspace, size_t workspace_bytes, ssd_stream_t stream);
+
+/* Backward (reverse mode of ssd_fwd for the upstream gradients dy and,
+ * if SSD_HAS_DFINAL, dfinal_states).  The forward intermediates are
+ * recomputed inside (the call is stateless).  Gradients are overwritten, not
+ * accumulated: dx, ddt, dB, dC in dtype; ddt_bias, dA, dD (H) fp32;
+ * dinitial_states (fp32) iff SSD_WANT_DINIT.  All reductions (dA, dD,
+ * ddt_bias over tokens, dB and dC over the heads of a group) are taken in a
+ * fixed order: results are bitwise reproducible run to run. */
+int ssd_bwd(const ssd_problem* prob, const void* x, const void* dt, const float* dt_bias,
+            const float* A, const void* B, const void* C, const float* D,
+            const float* initial_states, const int32_t* seq_idx, const void* dy,
+            const float* dfinal_states, void* dx, void* ddt, float* ddt_bias, float* dA,
+            void* dB, void* dC, float* dD, float* dinitial_states, void* workspace,
+            size_t workspace_bytes, ssd_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* ssd_status_string(int status);
+
+/* Synchronises `stream`, then reads the device status word of the last call
+ * that used `workspace` (SSD_OK or SSD_ERR_TIMEOUT).  Returns SSD_ERR_CUDA if
+ * the synchronisation or the copy fails. */
+int ssd_read_device_status(const void* workspace, ssd_stream_t stream);
+
+/* Library build/version string, e.g. "libssd 0.1 sm_103a". */
+const char* ssd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_H_ */

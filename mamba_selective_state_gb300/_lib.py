@@ -1,0 +1,144 @@
+"""Thin ctypes binding over libssd (include/ssd.h): the same entry points,
+argument marshalling only.  Every step of the layer runs in the library's
+CUDA kernels; there is no fallback of any kind -- if libssd.so is missing or
+does not load, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssd.so")
+
+SSD_OK = 0
+SSD_ERR_INVALID_ARGUMENT = 1
+SSD_ERR_UNSUPPORTED = 2
+SSD_ERR_WORKSPACE_TOO_SMALL = 3
+SSD_ERR_CUDA = 4
+SSD_ERR_TIMEOUT = 5
+SSD_F32 = 0
+SSD_BF16 = 1
+SSD_HAS_INIT = 1
+SSD_HAS_SEQ_IDX = 2
+SSD_HAS_DFINAL = 4
+SSD_WANT_DINIT = 8
+SSD_TEST_DROP_SCAN_PUBLISH = 1 << 16
+
+# every symbol include/ssd.h declares
+EXPORTS = ["ssd_fwd_workspace_bytes", "ssd_bwd_workspace_bytes", "ssd_fwd", "ssd_bwd",
+           "ssd_status_string", "ssd_read_device_status", "ssd_version"]
+
+
+class ssd_problem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+                ("nheads", ctypes.c_int64), ("headdim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+                ("chunk_size", ctypes.c_int64), ("dtype", ctypes.c_int32),
+                ("flags", ctypes.c_int32)]
+
+
+class SSDError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (code {code})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libssd.so not built at {LIB_PATH}; run "
+                          "`python -m mamba_selective_state_gb300.build_ext`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    pp = ctypes.POINTER(ssd_problem)
+    lib.ssd_fwd_workspace_bytes.argtypes = [pp]
+    lib.ssd_fwd_workspace_bytes.restype = sz
+    lib.ssd_bwd_workspace_bytes.argtypes = [pp]
+    lib.ssd_bwd_workspace_bytes.restype = sz
+    lib.ssd_fwd.argtypes = [pp] + [vp] * 11 + [vp, sz, vp]
+    lib.ssd_fwd.restype = i32
+    lib.ssd_bwd.argtypes = [pp] + [vp] * 19 + [vp, sz, vp]
+    lib.ssd_bwd.restype = i32
+    lib.ssd_status_string.argtypes = [i32]
+    lib.ssd_status_string.restype = ctypes.c_char_p
+    lib.ssd_read_device_status.argtypes = [vp, vp]
+    lib.ssd_read_device_status.restype = i32
+    lib.ssd_version.restype = ctypes.c_char_p
+    return lib
+
+
+LIB = _load()
+
+
+def status_string(code: int) -> str:
+    return LIB.ssd_status_string(int(code)).decode()
+
+
+def version() -> str:
+    return LIB.ssd_version().decode()
+
+
+def make_problem(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, dtype,
+                 flags=0) -> ssd_problem:
+    if isinstance(dtype, torch.dtype):
+        dtype = SSD_BF16 if dtype == torch.bfloat16 else SSD_F32
+    return ssd_problem(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, dtype, flags)
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def ssd_fwd_workspace_bytes(prob: ssd_problem) -> int:
+    return int(LIB.ssd_fwd_workspace_bytes(ctypes.byref(prob)))
+
+
+def ssd_bwd_workspace_bytes(prob: ssd_problem) -> int:
+    return int(LIB.ssd_bwd_workspace_bytes(ctypes.byref(prob)))
+
+
+def ssd_fwd(prob, x, dt, dt_bias, A, B, C, D, initial_states, seq_idx, y, final_states,
+            workspace, workspace_bytes=None, stream=None, check=True) -> int:
+    """Enqueue the forward on ``stream`` (default: torch's current stream).
+    Tensor arguments may also be raw device addresses (ints)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = LIB.ssd_fwd(ctypes.byref(prob), _p(x), _p(dt), _p(dt_bias), _p(A), _p(B), _p(C), _p(D),
+                     _p(initial_states), _p(seq_idx), _p(y), _p(final_states), _p(workspace),
+                     workspace_bytes, _stream(stream))
+    if check and rc != SSD_OK:
+        raise SSDError(rc, "ssd_fwd")
+    return rc
+
+
+def ssd_bwd(prob, x, dt, dt_bias, A, B, C, D, initial_states, seq_idx, dy, dfinal_states,
+            dx, ddt, ddt_bias, dA, dB, dC, dD, dinitial_states, workspace,
+            workspace_bytes=None, stream=None, check=True) -> int:
+    """Enqueue the backward on ``stream`` (default: torch's current stream)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = LIB.ssd_bwd(ctypes.byref(prob), _p(x), _p(dt), _p(dt_bias), _p(A), _p(B), _p(C), _p(D),
+                     _p(initial_states), _p(seq_idx), _p(dy), _p(dfinal_states), _p(dx), _p(ddt),
+                     _p(ddt_bias), _p(dA), _p(dB), _p(dC), _p(dD), _p(dinitial_states),
+                     _p(workspace), workspace_bytes, _stream(stream))
+    if check and rc != SSD_OK:
+        raise SSDError(rc, "ssd_bwd")
+    return rc
+
+
+def ssd_read_device_status(workspace, stream=None) -> int:
+    return int(LIB.ssd_read_device_status(_p(workspace), _stream(stream)))

@@ -1,0 +1,210 @@
+// k_state_passing.cu -- cross-chunk state passing as a single-pass associative
+// scan (forward and reverse), HBM-bound.
+//
+// Page "B200 Helion Mamba-2" (aitrends.kr/articles/109906), section "Helion
+// based B200 kernel redesign": the sequential chunk loops of the forward and
+// backward state passing are replaced by an associative scan.  Page
+// "llm-mamba-200" (gigipick.blogspot.com), section 2: the pairs (a, b) of the
+// recurrence h <- a h + b combine associatively,
+//     (a, b) o (a', b') = (a a', a' b + b'),
+// so the carry-in state of every chunk is an exclusive prefix of the pairs
+// (a_c, S_c) applied to the initial state.
+//
+// Forward:   H_in[0] = init (or 0),   H_in[c+1] = a_c H_in[c] + S_c,   final = H_in[nc]
+// Backward:  G[nc] = dfinal (or 0),   G[c] = dHloc[c] + a_c G[c+1],
+//            dS[c] = G[c+1],          dinit = G[0]
+// The backward is the same scan run over the chunks in reverse order.
+//
+// Decomposition.  A tile is (row b, head h, a block of 1024 consecutive state
+// elements, a segment of kSpSeg consecutive chunks).  Each thread owns 4
+// consecutive elements (one float4, coalesced across the CTA) and scans its
+// segment sequentially -- work-efficient, the loads do not depend on the
+// carry and are all issued up front.  Segments are joined by decoupled
+// lookback: a tile publishes its aggregate pair (the product of the decays, the
+// locally scanned state) as soon as it has it, then walks back over its
+// predecessors, folding aggregates until it meets a published inclusive
+// prefix.  Tiles take their index from an atomic ticket, so every tile a
+// tile waits on is already resident: the waits always end.  Each wait is also
+// bounded in time; on expiry the tile records a timeout in the status word
+// and continues with a zero prefix instead of hanging.
+#include "ssd_internal.cuh"
+
+namespace ssd {
+
+namespace {
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;      // 2 s
+constexpr unsigned long long kTestWaitLimitNs = 100000000ull;   // 0.1 s
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ float4 fma4(float a, float4 x, float4 y) {
+  return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
+}
+
+enum : int { kFlagNone = 0, kFlagAggregate = 1, kFlagPrefix = 2 };
+
+template <bool kBwd>
+__global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs f) {
+  __shared__ int s_ticket, s_flag;
+  int* flags = kBwd ? f.flags_bwd : f.flags_fwd;
+  if (threadIdx.x == 0) s_ticket = atomicAdd(kBwd ? &f.hdr->ticket_bwd : &f.hdr->ticket_fwd, 1);
+  __syncthreads();
+  const int ticket = s_ticket;
+  const int seg = ticket / p.sp_chains;
+  const int chain = ticket - seg * p.sp_chains;
+  const int eblk = chain % p.sp_neblk;
+  const long long bh = chain / p.sp_neblk;  // bi * H + h
+  const int e = eblk * kSpElems + threadIdx.x * 4;
+  const bool active = e < p.PN;
+  const int k0 = seg * kSpSeg;
+  const int nk = min(kSpSeg, p.nc - k0);
+  const float* achunk = f.achunk + bh * p.nc;
+  const float* in = f.S;                 // forward: chunk states; backward: dHloc
+  float* out = kBwd ? f.S : f.Hin;       // forward: carry-in states; backward: dS (in place)
+  const size_t lb_slot = ((size_t)chain * p.sp_nseg + seg) * kSpElems + threadIdx.x * 4;
+  const unsigned long long limit =
+      (p.flags & SSD_TEST_DROP_SCAN_PUBLISH) ? kTestWaitLimitNs : kWaitLimitNs;
+
+  // 1) local scan of the segment from a zero state; v[k] becomes the value
+  //    entering chunk k, dprod[k] the product of the decays before chunk k.
+  float4 v[kSpSeg];
+  float dprod[kSpSeg];
+#pragma unroll
+  for (int k = 0; k < kSpSeg; ++k) {
+    v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (k < nk && active) {
+      const int c = kBwd ? p.nc - 1 - (k0 + k) : k0 + k;
+      v[k] = __ldcs(reinterpret_cast<const float4*>(in + ((size_t)bh * p.nc + c) * p.PN + e));
+    }
+  }
+  float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+  float aprod = 1.0f;
+#pragma unroll
+  for (int k = 0; k < kSpSeg; ++k) {
+    if (k < nk) {
+      const int c = kBwd ? p.nc - 1 - (k0 + k) : k0 + k;
+      const float a = __ldg(achunk + c);
+      const float4 x = v[k];
+      v[k] = run;
+      dprod[k] = aprod;
+      run = fma4(a, run, x);
+      aprod *= a;
+    }
+  }
+
+  // 2) join with the predecessors
+  float4 prefix = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (seg == 0) {
+    const float* start = kBwd ? f.dfinal : f.init;
+    if (start != nullptr && active)
+      prefix = *reinterpret_cast<const float4*>(start + bh * p.PN + e);
+  } else {
+    if (active) __stcg(reinterpret_cast<float4*>(f.agg + lb_slot), run);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) st_release(flags + (size_t)chain * p.sp_nseg + seg, kFlagAggregate);
+    float acc_a = 1.0f;
+    float4 acc_v = make_float4(0.f, 0.f, 0.f, 0.f);
+    int sp = seg - 1;
+    bool joined = false;
+    while (sp >= 0) {
+      if (threadIdx.x == 0) {
+        const int* fp = flags + (size_t)chain * p.sp_nseg + sp;
+        int fl = ld_acquire(fp);
+        if (fl == kFlagNone) {
+          const unsigned long long t_start = global_ns();
+          while ((fl = ld_acquire(fp)) == kFlagNone) {
+            if (global_ns() - t_start > limit) {
+              atomicOr(&f.hdr->status, kDevTimeout);
+              fl = -1;
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+        __threadfence();
+        s_flag = fl;
+      }
+      __syncthreads();
+      const int fl = s_flag;
+      __syncthreads();
+      if (fl < 0) break;  // timed out: continue from what has been folded so far
+      const size_t slot = ((size_t)chain * p.sp_nseg + sp) * kSpElems + threadIdx.x * 4;
+      if (fl == kFlagPrefix) {
+        float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (active) pv = __ldcg(reinterpret_cast<const float4*>(f.incl + slot));
+        prefix = fma4(acc_a, pv, acc_v);
+        joined = true;
+        break;
+      }
+      // aggregate of segment sp: fold it under the spans already folded
+      float4 av = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (active) av = __ldcg(reinterpret_cast<const float4*>(f.agg + slot));
+      float a_sp = 1.0f;
+      const int ks = sp * kSpSeg, kn = min(kSpSeg, p.nc - ks);
+      for (int k = 0; k < kn; ++k) a_sp *= __ldg(achunk + (kBwd ? p.nc - 1 - (ks + k) : ks + k));
+      acc_v = fma4(acc_a, av, acc_v);
+      acc_a *= a_sp;
+      --sp;
+    }
+    if (!joined) {
+      if (sp < 0) {  // walked back to the chain start
+        const float* start = kBwd ? f.dfinal : f.init;
+        float4 sv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (start != nullptr && active) sv = *reinterpret_cast<const float4*>(start + bh * p.PN + e);
+        prefix = fma4(acc_a, sv, acc_v);
+      } else {
+        prefix = acc_v;  // timed out
+      }
+    }
+  }
+  const float4 incl = fma4(aprod, prefix, run);
+  const bool drop = (p.flags & SSD_TEST_DROP_SCAN_PUBLISH) && seg == 0 && chain == 0;
+  if (seg + 1 < p.sp_nseg && !drop) {
+    if (active) __stcg(reinterpret_cast<float4*>(f.incl + lb_slot), incl);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) st_release(flags + (size_t)chain * p.sp_nseg + seg, kFlagPrefix);
+  }
+
+  // 3) carry-in values of the segment's chunks, and the end of the chain
+  if (active) {
+#pragma unroll
+    for (int k = 0; k < kSpSeg; ++k) {
+      if (k < nk) {
+        const int c = kBwd ? p.nc - 1 - (k0 + k) : k0 + k;
+        *reinterpret_cast<float4*>(out + ((size_t)bh * p.nc + c) * p.PN + e) =
+            fma4(dprod[k], prefix, v[k]);
+      }
+    }
+    if (seg == p.sp_nseg - 1) {
+      float* fin = kBwd ? f.dinit : f.final_states;
+      if (fin != nullptr) *reinterpret_cast<float4*>(fin + bh * p.PN + e) = incl;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_state_passing(const Plan& p, const Bufs& f, bool backward, cudaStream_t s) {
+  const unsigned tiles = (unsigned)p.sp_chains * p.sp_nseg;
+  if (backward)
+    state_passing_kernel<true><<<tiles, kSpThreads, 0, s>>>(p, f);
+  else
+    state_passing_kernel<false><<<tiles, kSpThreads, 0, s>>>(p, f);
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

@@ -1,0 +1,134 @@
+// ssd_internal.cuh -- plan of one SSD problem (dimensions, workspace carve-up,
+// kernel tiling) shared by the host entry points and the kernels of libssd.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ssd.h"
+
+namespace ssd {
+
+// Status bits the kernels OR into the device status word.
+enum : int { kDevTimeout = 1 };
+
+// State-passing scan tiling: one CTA scans kSpElems consecutive state elements
+// (kSpThreads threads x 4 floats) over kSpSeg consecutive chunks.
+constexpr int kSpThreads = 256;
+constexpr int kSpElems = kSpThreads * 4;
+constexpr int kSpSeg = 8;
+
+// Workspace header (first 256 bytes): device status word, then the tile
+// tickets of the forward and backward state-passing scans.
+struct WsHeader {
+  int status;
+  int ticket_fwd;
+  int ticket_bwd;
+  int pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header size");
+
+struct Plan {
+  // dimensions
+  int b, L, H, P, N, G, Q, nc, PN, hpg;  // hpg = heads per group
+  int dtype, flags;
+  long long Lp;                          // nc * Q (padded tokens per row)
+  // state-passing scan tiling
+  int sp_neblk, sp_nseg, sp_chains;      // chains = b * H * neblk
+  // chunk-backward token blocks per chunk
+  int cb_ntb;
+  // workspace offsets in bytes (0 = absent)
+  size_t off_dte, off_lcs, off_achunk;   // (b,H,Lp) f32, (b,H,Lp) f32, (b,H,nc) f32
+  size_t off_S;                          // (b,H,nc,P,N) f32: chunk states / dHloc / dS
+  size_t off_Hin;                        // (b,H,nc,P,N) f32: carry-in states
+  size_t off_agg, off_incl;              // (chains, nseg, kSpElems) f32 each
+  size_t off_flags_fwd, off_flags_bwd;   // (chains, nseg) int32 each
+  // backward only
+  size_t off_dl, off_ddte;               // (b,H,Lp) f32 each
+  size_t off_udu;                        // (b,H,nc,cb_ntb) f32
+  size_t off_da;                         // (b,H,nc) f32
+  size_t off_pdA, off_pdb;               // (b,nc,H) f32 partials of dA, ddt_bias
+  size_t off_pdD;                        // (b,nc,cb_ntb,H) f32 partials of dD
+  size_t fwd_bytes, bwd_bytes;
+};
+
+// Device pointers of one call, passed by value to every kernel.
+struct Bufs {
+  const void* x;
+  const void* dt;
+  const float* dt_bias;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const float* init;
+  const int32_t* seq;
+  void* y;
+  float* final_states;
+  // backward
+  const void* dy;
+  const float* dfinal;
+  void* dx;
+  void* ddt;
+  float* ddt_bias;
+  float* dA;
+  void* dB;
+  void* dC;
+  float* dD;
+  float* dinit;
+  // workspace views
+  WsHeader* hdr;
+  float* dte;
+  float* lcs;
+  float* achunk;
+  float* S;
+  float* Hin;
+  float* agg;
+  float* incl;
+  int* flags_fwd;
+  int* flags_bwd;
+  float* dl;
+  float* ddte;
+  float* udu;
+  float* da;
+  float* pdA;
+  float* pdb;
+  float* pdD;
+};
+
+// Loads/stores of the storage dtype as fp32.
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// Segment id of token t of row bi (0 when there is no seq_idx).
+__device__ __forceinline__ int seg_of(const Plan& p, const Bufs& f, int bi, long long t) {
+  return (f.seq != nullptr) ? __ldg(f.seq + (long long)bi * p.L + t) : 0;
+}
+// Segment id live at the end of the previous chunk (token c*Q - 1; the first
+// chunk takes the id of token 0, so the initial state reaches segment 0).
+__device__ __forceinline__ int seg_in_of(const Plan& p, const Bufs& f, int bi, int c) {
+  long long t = (long long)c * p.Q - 1;
+  return seg_of(p, f, bi, t < 0 ? 0 : t);
+}
+
+// Host launchers (each returns the launch's cudaError_t).
+cudaError_t launch_dt_cumsum(const Plan& p, const Bufs& f, cudaStream_t s);
+cudaError_t launch_state_passing(const Plan& p, const Bufs& f, bool backward, cudaStream_t s);
+cudaError_t launch_chunk_state(const Plan& p, const Bufs& f, bool dstates, cudaStream_t s);
+cudaError_t launch_chunk_scan(const Plan& p, const Bufs& f, cudaStream_t s);
+cudaError_t launch_chunk_bwd(const Plan& p, const Bufs& f, cudaStream_t s);
+cudaError_t launch_dt_bwd(const Plan& p, const Bufs& f, cudaStream_t s);
+cudaError_t launch_param_reduce(const Plan& p, const Bufs& f, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace ssd

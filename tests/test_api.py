@@ -1,0 +1,119 @@
+"""The C-ABI library loads, exports every symbol include/ssd.h declares, and
+rejects bad arguments on the host before touching the device.  CPU only
+(the calls below return before any CUDA call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mamba_selective_state_gb300 import build_ext
+    build_ext.build()
+    from mamba_selective_state_gb300 import _lib
+    return _lib
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssd_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert set(names) == set(lib.EXPORTS)
+    for n in names:
+        assert hasattr(lib.LIB, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (ssd_\w+)", out))
+    assert set(names) <= exported
+
+
+def test_version_and_status_strings(lib):
+    assert "sm_103a" in lib.version()
+    for code in range(6):
+        assert lib.status_string(code) and lib.status_string(code) != "unknown status"
+    assert lib.status_string(99) == "unknown status"
+
+
+def prob(lib, **kw):
+    d = dict(batch=2, seqlen=300, nheads=8, headdim=64, dstate=128, ngroups=2, chunk_size=128,
+             dtype=lib.SSD_BF16, flags=0)
+    d.update(kw)
+    return lib.make_problem(**d)
+
+
+def test_workspace_sizes(lib):
+    p = prob(lib)
+    fw, bw = lib.ssd_fwd_workspace_bytes(p), lib.ssd_bwd_workspace_bytes(p)
+    assert 0 < fw < bw
+    # the fp32 chunk states and carry-in states dominate: 2 x (b H nc P N) floats
+    nc = 3
+    assert fw >= 2 * 2 * 8 * nc * 64 * 128 * 4
+    assert lib.ssd_fwd_workspace_bytes(prob(lib, seqlen=385)) > fw   # one more chunk
+
+
+@pytest.mark.parametrize("bad", [
+    dict(ngroups=3), dict(chunk_size=24), dict(chunk_size=512), dict(headdim=48),
+    dict(dstate=256), dict(headdim=128, dstate=128), dict(seqlen=0), dict(batch=0),
+    dict(dtype=7), dict(flags=1 << 5),
+])
+def test_invalid_problems_have_no_workspace(lib, bad):
+    assert lib.ssd_fwd_workspace_bytes(prob(lib, **bad)) == 0
+    assert lib.ssd_bwd_workspace_bytes(prob(lib, **bad)) == 0
+
+
+FAKE = 1 << 20  # an aligned address that is never dereferenced: validation fails first
+
+
+def fwd_call(lib, p, **over):
+    args = dict(x=FAKE, dt=FAKE, dt_bias=FAKE, A=FAKE, B=FAKE, C=FAKE, D=FAKE,
+                initial_states=None, seq_idx=None, y=FAKE, final_states=FAKE,
+                workspace=FAKE)
+    args.update(over)
+    ws = over.pop("workspace_bytes", 1 << 40)
+    return lib.ssd_fwd(p, args["x"], args["dt"], args["dt_bias"], args["A"], args["B"],
+                       args["C"], args["D"], args["initial_states"], args["seq_idx"], args["y"],
+                       args["final_states"], args["workspace"], workspace_bytes=ws, stream=0,
+                       check=False)
+
+
+def test_fwd_argument_errors(lib):
+    p = prob(lib)
+    assert lib.LIB.ssd_fwd(None, *([None] * 11), None, 0, None) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert fwd_call(lib, p, x=None) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert fwd_call(lib, p, workspace=None) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert fwd_call(lib, p, B=FAKE + 4) == lib.SSD_ERR_INVALID_ARGUMENT      # misaligned
+    assert fwd_call(lib, p, initial_states=FAKE) == lib.SSD_ERR_INVALID_ARGUMENT  # flag missing
+    pi = prob(lib, flags=lib.SSD_HAS_INIT)
+    assert fwd_call(lib, pi) == lib.SSD_ERR_INVALID_ARGUMENT                  # pointer missing
+    ps = prob(lib, flags=lib.SSD_HAS_SEQ_IDX)
+    assert fwd_call(lib, ps) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert fwd_call(lib, prob(lib, flags=lib.SSD_HAS_DFINAL)) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert fwd_call(lib, p, workspace_bytes=16) == lib.SSD_ERR_WORKSPACE_TOO_SMALL
+    assert fwd_call(lib, prob(lib, headdim=48)) == lib.SSD_ERR_UNSUPPORTED
+    assert fwd_call(lib, prob(lib, ngroups=3)) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert fwd_call(lib, prob(lib, seqlen=0)) == lib.SSD_ERR_INVALID_ARGUMENT
+
+
+def test_bwd_argument_errors(lib):
+    p = prob(lib, flags=lib.SSD_WANT_DINIT)
+    args = [FAKE] * 7 + [None, None, FAKE, None] + [FAKE] * 7 + [None, FAKE]
+    # WANT_DINIT without a dinitial_states pointer
+    rc = lib.ssd_bwd(p, *args, workspace_bytes=1 << 40, stream=0, check=False)
+    assert rc == lib.SSD_ERR_INVALID_ARGUMENT
+    p = prob(lib)
+    args2 = list(args)
+    args2[11] = None  # dx missing
+    rc = lib.ssd_bwd(p, *args2, workspace_bytes=1 << 40, stream=0, check=False)
+    assert rc == lib.SSD_ERR_INVALID_ARGUMENT
+    rc = lib.ssd_bwd(p, *args, workspace_bytes=1024, stream=0, check=False)
+    assert rc == lib.SSD_ERR_WORKSPACE_TOO_SMALL
