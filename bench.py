@@ -1,0 +1,442 @@
+"""Benchmark of the Mamba-2 SSD layer (ssd_fwd + ssd_bwd) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference] [--no-cpu-baseline]
+
+A step is one pass of the whole layer -- ssd_fwd then ssd_bwd through the C
+ABI -- over one batch of the workload, inputs resident in HBM.  L2 is flushed
+(a 256 MB write) between steps, outside the timed events; each step is timed
+with CUDA events on the launching stream.  Under torchrun every rank runs its
+own copy of the workload (independent problems, no collective): weak scaling,
+``value`` = tokens of all ranks / max over ranks of the timed region.
+
+``--impl reference`` times the float64 CPU oracle instead (rank 0 only), each
+step a bounded prefix of the same workload.
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SSD layer fwd+bwd tokens/s (ms) at b2·L8192 bf16; % of HBM / tensor roofline"
+DEFAULT_WORKLOAD = "b2_L8192_bf16"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes and flops per launch (the per-unit figures, times the units
+# of one launch; the design doc states the same formulas)
+# ----------------------------------------------------------------------------
+def kernel_model(cfg, dtype_bytes):
+    b, L, H, P, N, G, Q = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate",
+                                             "ngroups", "chunk"))
+    nc = -(-L // Q)
+    Lp = nc * Q
+    s = dtype_bytes
+    T = b * L
+    tokx = T * H * P * s          # one (b,L,H,P) tensor in dtype
+    tokbc = T * G * N * s         # one (b,L,G,N) tensor in dtype
+    st32 = b * H * nc * P * N * 4  # one fp32 chunk-state tensor
+    per_tok = b * H * Lp * 4      # one fp32 per-token-per-head vector
+    units = b * H * nc            # (row, head, chunk) tiles
+    gunits = b * G * nc           # (row, group, chunk) tiles
+    m = {}
+    m["dt_cumsum"] = dict(bytes=T * H * s + 2 * per_tok, flops=0)
+    m["chunk_state"] = dict(bytes=tokx + tokbc + 2 * per_tok + st32, flops=2 * units * Q * P * N)
+    m["state_passing_fwd"] = dict(bytes=2 * st32, flops=2 * units * P * N)
+    m["chunk_scan"] = dict(bytes=2 * tokx + 2 * tokbc + st32 + 2 * per_tok,
+                           flops=gunits * 2 * Q * Q * N + units * (2 * Q * Q * P + 2 * Q * N * P))
+    m["chunk_dstate"] = dict(bytes=tokx + tokbc + per_tok + st32, flops=2 * units * Q * P * N)
+    m["state_passing_bwd"] = dict(bytes=2 * st32, flops=2 * units * P * N)
+    m["chunk_bwd"] = dict(bytes=3 * tokx + 4 * tokbc + 2 * st32 + 4 * per_tok,
+                          flops=gunits * 2 * Q * Q * N
+                          + units * (8 * Q * P * N + 4 * Q * Q * P + 4 * Q * Q * N))
+    m["dt_bwd"] = dict(bytes=2 * T * H * s + 4 * per_tok, flops=0)
+    m["param_reduce"] = dict(bytes=b * nc * H * 4 * 4, flops=0)
+    # compulsory IO of the layer (fwd reads x dt B C, writes y; bwd reads x dt
+    # B C dy, writes dx ddt dB dC)
+    layer_io = (tokx + T * H * s + 2 * tokbc + tokx) + (2 * tokx + T * H * s + 2 * tokbc
+                                                        + tokx + T * H * s + 2 * tokbc)
+    return m, layer_io
+
+
+def base_name(kname):
+    for suf in ("_simt", "_tc"):
+        if kname.endswith(suf):
+            return kname[: -len(suf)]
+    return kname
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as fh:
+            pk = json.load(fh)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (the baseline and the reference arm)
+# ----------------------------------------------------------------------------
+class OracleSample:
+    """Bounded prefix sample of a workload for the oracle, calibrated so that
+    one fwd+bwd takes about ``target_s`` seconds."""
+
+    def __init__(self, name, target_s):
+        from mamba_selective_state_gb300.inputs import make_workload
+        from oracle import ssd_ref
+        self.name = name
+        self.full = make_workload(name, seed=0, dfinal=False)
+        self.f = {n: self.full.f64(n) for n in ["x", "dt", "dt_bias", "A", "B", "C", "D", "dy",
+                                                 "initial_states", "seq_idx"]}
+        ssd_ref.build_oracle()
+        probe = max(16, min(self.full.seqlen, 64))
+        t = self.run(probe)[0]
+        per_tok = max(t / probe, 1e-7)
+        self.Lp = int(max(16, min(self.full.seqlen, target_s / per_tok)))
+
+    def run(self, Lp):
+        from oracle import ssd_ref
+        cut = lambda a: None if a is None else a[:, :Lp]  # noqa: E731
+        a = dict(self.f)
+        for n in ("x", "dt", "B", "C", "dy", "seq_idx"):
+            a[n] = cut(a[n])
+        args = [a[n] for n in ["x", "dt", "dt_bias", "A", "B", "C", "D"]]
+        kw = dict(initial_states=a["initial_states"], seq_idx=a["seq_idx"])
+        t0 = time.perf_counter()
+        ssd_ref.ssd_fwd(*args, **kw)
+        th_f = ssd_ref.last_threads()
+        ssd_ref.ssd_bwd(*args, a["dy"], **kw)
+        th_b = ssd_ref.last_threads()
+        return time.perf_counter() - t0, max(th_f, th_b)
+
+    def describe(self):
+        return (f"float64 oracle fwd+bwd on the first {self.Lp} of {self.full.seqlen} tokens of "
+                f"every row ({self.full.batch} rows, all {self.full.nheads} heads) of {self.name}")
+
+
+def cpu_baseline(name, target_s=15.0):
+    smp = OracleSample(name, target_s)
+    secs, threads = smp.run(smp.Lp)
+    tok = smp.full.batch * smp.Lp
+    return {"value": tok / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": smp.describe(), "seconds": secs}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    total_budget = 150.0
+    per_step = max(0.2, min(10.0, total_budget / max(1, args.steps + args.warmup)))
+    smp = OracleSample(args.workload, per_step)
+    for _ in range(args.warmup):
+        smp.run(smp.Lp)
+    times, threads = [], 1
+    for _ in range(args.steps):
+        t, threads = smp.run(smp.Lp)
+        times.append(t)
+    tot = sum(times)
+    tok = smp.full.batch * smp.Lp * len(times)
+    value = tok / tot
+    cfg = workload_config(args.workload)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": smp.describe()},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(name):
+    from mamba_selective_state_gb300.inputs import WORKLOADS
+    cfg = dict(WORKLOADS[name])
+    out = {"workload": name}
+    out.update({k: v for k, v in cfg.items() if k != "dtype"})
+    return out
+
+
+# ----------------------------------------------------------------------------
+def run_gpu(args, world, rank, local):
+    import torch
+    from mamba_selective_state_gb300 import _lib
+    from mamba_selective_state_gb300.inputs import make_workload
+    from mamba_selective_state_gb300.runner import SSDDevice
+
+    inp = make_workload(args.workload, seed=rank, dfinal=False)
+    dev = SSDDevice(inp, device=f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev.device)
+
+    def step():
+        dev.fwd(stream=stream)
+        dev.bwd(stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dev.device_status(stream) != 0:
+        raise RuntimeError("device status word reports an error after warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    _lib.profile_start()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    prof = _lib.profile_stop()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    tot_ms = sum(step_ms)
+    tot_ms_max = max_over_ranks(world, tot_ms)
+    if dev.device_status(stream) != 0:
+        raise RuntimeError("device status word reports an error in the timed region")
+
+    tokens = inp.batch * inp.seqlen
+    value = world * tokens * args.steps / (tot_ms_max / 1e3)
+
+    # ---- end to end: pinned host inputs -> device, fwd+bwd, results -> host
+    e2e = run_e2e(inp, dev, args, stream)
+
+    # ---- roofline of the dominant kernel
+    peaks, src = load_peaks()
+    cfg = workload_config(args.workload)
+    s_bytes = 2 if inp.dtype == "bf16" else 4
+    model, layer_io = kernel_model(dict(cfg, batch=inp.batch, seqlen=inp.seqlen), s_bytes)
+    kernels = {k: {"launches": n, "ms_per_launch": ms / n} for k, (n, ms) in prof.items()
+               if not k.startswith("_")}
+    launches = sum(v["launches"] for v in kernels.values())
+    dom = max(kernels, key=lambda k: kernels[k]["launches"] * kernels[k]["ms_per_launch"])
+    dm = model[base_name(dom)]
+    dur_s = kernels[dom]["ms_per_launch"] / 1e3
+    hbm_peak = peaks["hbm_gbs"]
+    tc_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    ach_gbs = dm["bytes"] / dur_s / 1e9
+    ach_tfs = dm["flops"] / dur_s / 1e12
+    if dom.endswith("_simt") and dm["flops"] > 0:
+        # FP32 FMA on the CUDA cores: 152 SMs x 128 lanes x 2 flop x max SM clock
+        alu_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": ach_tfs, "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": ach_tfs / alu_peak, "traffic": None, "kernel": dom,
+                "peak_source": "derived: 152 SM x 128 FP32 lanes x 2 x max SM clock"}
+    elif dm["flops"] and dm["flops"] / dm["bytes"] > tc_peak * 1e12 / (hbm_peak * 1e9):
+        roof = {"bound": "tensor", "achieved": ach_tfs, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": ach_tfs / tc_peak, "traffic": None, "kernel": dom,
+                "peak_source": f"{src} bf16_tflops_sustained"}
+    else:
+        roof = {"bound": "hbm", "achieved": ach_gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": ach_gbs / hbm_peak, "traffic": None, "kernel": dom,
+                "peak_source": f"{src} hbm_gbs"}
+    roof["algorithmic_bytes"] = dm["bytes"]
+    roof["algorithmic_flops"] = dm["flops"]
+    roof["ms_per_launch"] = kernels[dom]["ms_per_launch"]
+    for k, v in kernels.items():
+        mk = model.get(base_name(k))
+        if mk:
+            d = v["ms_per_launch"] / 1e3
+            v["GBps"] = mk["bytes"] / d / 1e9
+            v["TFLOPps"] = mk["flops"] / d / 1e12
+    ms_per_step = tot_ms_max / args.steps
+    layer = {"compulsory_io_bytes": layer_io,
+             "achieved_GBps": layer_io / (ms_per_step / 1e3) / 1e9,
+             "frac_of_hbm": layer_io / (ms_per_step / 1e3) / 1e9 / hbm_peak}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": inp.dtype, "data": "synthetic",
+            "config": dict(cfg, l2="flushed between steps (256 MB write, outside the events); "
+                                   "inputs larger than L2", parallelism="replicas" if world > 1
+                           else "single GPU"),
+            "roofline": roof, "layer_roofline": layer, "e2e": e2e,
+            "gpu_launches": launches, "kernels": kernels, "clocks": clk,
+            "wall_s_timed": t_wall}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload)
+    return line
+
+
+def run_e2e(inp, dev, args, stream):
+    """The same step through the public call with host buffers: pinned host
+    inputs copied in, fwd+bwd, results copied back, all inside the events."""
+    import torch
+    names_in = ["x", "dt", "B", "C", "dy", "dt_bias", "A", "D"]
+    if dev.init is not None:
+        names_in.append("init")
+    if dev.seq_idx is not None:
+        names_in.append("seq_idx")
+    host_in = {n: getattr(dev, n).to("cpu").pin_memory() for n in names_in}
+    names_out = ["y", "final", "dx", "ddt", "dB", "dC", "dA", "dD", "ddt_bias"]
+    host_out = {n: torch.empty_like(getattr(dev, n), device="cpu").pin_memory() for n in names_out}
+    bi = sum(t.numel() * t.element_size() for t in host_in.values())
+    bo = sum(t.numel() * t.element_size() for t in host_out.values())
+    steps = max(3, min(args.steps, 10))
+    for it in range(steps + 2):
+        if it == 2:
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        for n, t in host_in.items():
+            getattr(dev, n).copy_(t, non_blocking=True)
+        dev.fwd(stream=stream)
+        dev.bwd(stream=stream)
+        for n, t in host_out.items():
+            t.copy_(getattr(dev, n), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    tokens = inp.batch * inp.seqlen
+    return {"value": tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":  # host-only: rank 0 runs, the other ranks exit
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+        return
+    world, rank, local = dist_setup(args)
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    barrier(world)
+    if world > 1 and rank != 0:
+        __graft_entry__.build()
+    line = run_gpu(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -39,8 +39,9 @@
  *
  * Ownership: the caller allocates every buffer, the workspace included, and
  * keeps them alive until the stream work completes.  The library never
- * allocates, never synchronises (except ssd_read_device_status) and keeps no
- * mutable global state other than a per-device cache of device attributes.
+ * allocates, never synchronises (except ssd_read_device_status and
+ * ssd_profile_stop) and keeps no mutable global state other than a
+ * per-device cache of device attributes and the optional timing records.
  * Calls enqueue work on the given stream and return before it completes.
  *
  * Errors: every entry point validates its arguments before enqueuing
@@ -134,6 +135,20 @@ int ssd_read_device_status(const void* workspace, ssd_stream_t stream);
 
 /* Library build/version string, e.g. "libssd 0.1 sm_103a". */
 const char* ssd_version(void);
+
+/* Per-kernel timing, a measurement aid.  ssd_profile_start (re)starts
+ * recording on the current device: from then on every kernel launched by
+ * ssd_fwd/ssd_bwd is bracketed by two CUDA events recorded on the call's
+ * stream.  ssd_profile_stop ends recording and waits for the recorded events
+ * (it synchronises), folding them into per-kernel totals that
+ * ssd_profile_count/ssd_profile_get report (name is a static string).  The
+ * event pool holds 8192 launches; ssd_profile_stop returns
+ * SSD_ERR_WORKSPACE_TOO_SMALL if launches beyond it went unrecorded.  Use
+ * from one host thread. */
+int ssd_profile_start(void);
+int ssd_profile_stop(void);
+int ssd_profile_count(void);
+int ssd_profile_get(int index, const char** name, int* launches, double* total_ms);
 
 #ifdef __cplusplus
 }

@@ -29,7 +29,8 @@ SSD_TEST_DROP_SCAN_PUBLISH = 1 << 16
 
 # every symbol include/ssd.h declares
 EXPORTS = ["ssd_fwd_workspace_bytes", "ssd_bwd_workspace_bytes", "ssd_fwd", "ssd_bwd",
-           "ssd_status_string", "ssd_read_device_status", "ssd_version"]
+           "ssd_status_string", "ssd_read_device_status", "ssd_version", "ssd_profile_start",
+           "ssd_profile_stop", "ssd_profile_count", "ssd_profile_get"]
 
 
 class ssd_problem(ctypes.Structure):
@@ -66,6 +67,12 @@ def _load():
     lib.ssd_read_device_status.argtypes = [vp, vp]
     lib.ssd_read_device_status.restype = i32
     lib.ssd_version.restype = ctypes.c_char_p
+    lib.ssd_profile_start.restype = i32
+    lib.ssd_profile_stop.restype = i32
+    lib.ssd_profile_count.restype = i32
+    lib.ssd_profile_get.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p),
+                                    ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)]
+    lib.ssd_profile_get.restype = i32
     return lib
 
 
@@ -142,3 +149,24 @@ def ssd_bwd(prob, x, dt, dt_bias, A, B, C, D, initial_states, seq_idx, dy, dfina
 
 def ssd_read_device_status(workspace, stream=None) -> int:
     return int(LIB.ssd_read_device_status(_p(workspace), _stream(stream)))
+
+
+def profile_start() -> None:
+    rc = LIB.ssd_profile_start()
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_profile_start")
+
+
+def profile_stop() -> dict:
+    """Stop per-kernel timing; returns {kernel name: (launches, total ms)}."""
+    rc = LIB.ssd_profile_stop()
+    if rc not in (SSD_OK, SSD_ERR_WORKSPACE_TOO_SMALL):
+        raise SSDError(rc, "ssd_profile_stop")
+    out = {}
+    for i in range(LIB.ssd_profile_count()):
+        name, n, ms = ctypes.c_char_p(), ctypes.c_int(), ctypes.c_double()
+        if LIB.ssd_profile_get(i, ctypes.byref(name), ctypes.byref(n), ctypes.byref(ms)) == SSD_OK:
+            out[name.value.decode()] = (int(n.value), float(ms.value))
+    if rc == SSD_ERR_WORKSPACE_TOO_SMALL:
+        out["_dropped"] = (1, 0.0)
+    return out

@@ -77,8 +77,8 @@ __global__ void __launch_bounds__(kThreads) chunk_state_simt(Plan p, Bufs f) {
 #pragma unroll
     for (int k = 0; k < kMaxOut; ++k) {
       if (k < nout) {
-        const int o = threadIdx.x + k * kThreads;
-        const int pp = o / N, n = o - pp * N;
+        const int o = threadIdx.x + k * kThreads;  // o = n * P + p
+        const int n = o / P, pp = o - n * P;
         float a = acc[k];
         for (int j = 0; j < kJs; ++j) a = fmaf(Xs[j * P + pp], Bs[j * N + n], a);
         acc[k] = a;
@@ -117,10 +117,10 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_simt(Plan p, Bufs f) {
     dq[i] = f.dte[bh * p.Lp + t0 + i];
     sq[i] = i < len ? seg_of(p, f, bi, (long long)t0 + i) : -1;
   }
-  const float* hin = f.Hin + (bh * p.nc + c) * p.PN;
+  const T* hin = static_cast<const T*>(f.Hin) + (bh * p.nc + c) * p.PN;
   for (int idx = threadIdx.x; idx < p.PN; idx += kThreads) {
-    const int pp = idx / N, n = idx - pp * N;
-    Hs[pp * N1 + n] = hin[idx];
+    const int n = idx / P, pp = idx - n * P;
+    Hs[pp * N1 + n] = to_f(hin[idx]);
   }
   const int s_in = seg_in_of(p, f, bi, c);
   const float Dh = f.D[h];
@@ -287,12 +287,12 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt(Plan p, Bufs f) {
       lq[i] = f.lcs[bh * p.Lp + t0 + i];
       dq[i] = f.dte[bh * p.Lp + t0 + i];
     }
-    const float* dsg = f.S + (bh * p.nc + c) * p.PN;
-    const float* hg = f.Hin + (bh * p.nc + c) * p.PN;
+    const T* dsg = static_cast<const T*>(f.dS) + (bh * p.nc + c) * p.PN;
+    const T* hg = static_cast<const T*>(f.Hin) + (bh * p.nc + c) * p.PN;
     for (int idx = threadIdx.x; idx < p.PN; idx += kThreads) {
-      const int pp = idx / N, n = idx - pp * N;
-      dSs[pp * N1 + n] = dsg[idx];
-      Hs[pp * N1 + n] = hg[idx];
+      const int n = idx / P, pp = idx - n * P;
+      dSs[pp * N1 + n] = to_f(dsg[idx]);
+      Hs[pp * N1 + n] = to_f(hg[idx]);
     }
     for (int idx = threadIdx.x; idx < kTb * P; idx += kThreads) {
       const int j = idx / P, pp = idx - j * P;
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt(Plan p, Bufs f) {
     if (tb == 0) {  // dL/da_c = <dS, H_in[c]>, folded in a fixed order
       float s = 0.0f;
       for (int idx = threadIdx.x; idx < p.PN; idx += kThreads) {
-        const int pp = idx / N, n = idx - pp * N;
+        const int n = idx / P, pp = idx - n * P;
         s = fmaf(dSs[pp * N1 + n], Hs[pp * N1 + n], s);
       }
       __syncthreads();
@@ -551,8 +551,10 @@ cudaError_t launch_with_smem(K kernel, dim3 grid, size_t smem, cudaStream_t s, c
 }  // namespace
 
 cudaError_t launch_chunk_state(const Plan& p, const Bufs& f, bool dstates, cudaStream_t s) {
+  if (chunk_state_tc_supported(p)) return launch_chunk_state_tc(p, f, dstates, s);
   dim3 grid(p.nc, p.H, p.b);
   const size_t smem = chunk_state_smem(p);
+  set_kernel_name(dstates ? "chunk_dstate_simt" : "chunk_state_simt");
   if (p.dtype == SSD_BF16)
     return dstates ? launch_with_smem(chunk_state_simt<__nv_bfloat16, true>, grid, smem, s, p, f)
                    : launch_with_smem(chunk_state_simt<__nv_bfloat16, false>, grid, smem, s, p, f);
@@ -561,15 +563,19 @@ cudaError_t launch_chunk_state(const Plan& p, const Bufs& f, bool dstates, cudaS
 }
 
 cudaError_t launch_chunk_scan(const Plan& p, const Bufs& f, cudaStream_t s) {
+  if (chunk_scan_tc_supported(p)) return launch_chunk_scan_tc(p, f, s);
   dim3 grid(p.nc, p.H, p.b);
   const size_t smem = chunk_scan_smem(p);
+  set_kernel_name("chunk_scan_simt");
   if (p.dtype == SSD_BF16) return launch_with_smem(chunk_scan_simt<__nv_bfloat16>, grid, smem, s, p, f);
   return launch_with_smem(chunk_scan_simt<float>, grid, smem, s, p, f);
 }
 
 cudaError_t launch_chunk_bwd(const Plan& p, const Bufs& f, cudaStream_t s) {
+  if (chunk_bwd_tc_supported(p)) return launch_chunk_bwd_tc(p, f, s);
   dim3 grid(p.cb_ntb, p.nc, p.b * p.G);
   const size_t smem = chunk_bwd_smem(p);
+  set_kernel_name("chunk_bwd_simt");
   if (p.dtype == SSD_BF16) return launch_with_smem(chunk_bwd_simt<__nv_bfloat16>, grid, smem, s, p, f);
   return launch_with_smem(chunk_bwd_simt<float>, grid, smem, s, p, f);
 }

@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(256) param_reduce_kernel(Plan p, Bufs f) {
 }  // namespace
 
 cudaError_t launch_dt_cumsum(const Plan& p, const Bufs& f, cudaStream_t s) {
+  set_kernel_name("dt_cumsum");
   dim3 grid(p.nc, p.b, (p.H + kHeadsPerCta - 1) / kHeadsPerCta);
   if (p.dtype == SSD_BF16)
     dt_cumsum_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p, f);
@@ -211,6 +212,7 @@ cudaError_t launch_dt_cumsum(const Plan& p, const Bufs& f, cudaStream_t s) {
 }
 
 cudaError_t launch_dt_bwd(const Plan& p, const Bufs& f, cudaStream_t s) {
+  set_kernel_name("dt_bwd");
   dim3 grid(p.nc, p.b, (p.H + kHeadsPerCta - 1) / kHeadsPerCta);
   if (p.dtype == SSD_BF16)
     dt_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p, f);
@@ -220,6 +222,7 @@ cudaError_t launch_dt_bwd(const Plan& p, const Bufs& f, cudaStream_t s) {
 }
 
 cudaError_t launch_param_reduce(const Plan& p, const Bufs& f, cudaStream_t s) {
+  set_kernel_name("param_reduce");
   param_reduce_kernel<<<p.H, 256, 0, s>>>(p, f);
   return cudaGetLastError();
 }

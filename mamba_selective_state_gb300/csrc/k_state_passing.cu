@@ -13,6 +13,7 @@
 // Forward:   H_in[0] = init (or 0),   H_in[c+1] = a_c H_in[c] + S_c,   final = H_in[nc]
 // Backward:  G[nc] = dfinal (or 0),   G[c] = dHloc[c] + a_c G[c+1],
 //            dS[c] = G[c+1],          dinit = G[0]
+// (dS goes to its own buffer; dHloc is read once).
 // The backward is the same scan run over the chunks in reverse order.
 //
 // Decomposition.  A tile is (row b, head h, a block of 1024 consecutive state
@@ -55,7 +56,33 @@ __device__ __forceinline__ float4 fma4(float a, float4 x, float4 y) {
 
 enum : int { kFlagNone = 0, kFlagAggregate = 1, kFlagPrefix = 2 };
 
-template <bool kBwd>
+// Public state tensors are (b, H, P, N); the chunk-state layout is (N, P):
+// the 4 consecutive elements e..e+3 (same n, headdim p..p+3) of a thread map
+// to public offsets (p+i)*N + n.
+__device__ __forceinline__ float4 load_public(const float* base, int e, int P, int N) {
+  const int n = e / P, pp = e - n * P;
+  return make_float4(base[(pp + 0) * N + n], base[(pp + 1) * N + n], base[(pp + 2) * N + n],
+                     base[(pp + 3) * N + n]);
+}
+__device__ __forceinline__ void store_public(float* base, int e, int P, int N, float4 v) {
+  const int n = e / P, pp = e - n * P;
+  base[(pp + 0) * N + n] = v.x;
+  base[(pp + 1) * N + n] = v.y;
+  base[(pp + 2) * N + n] = v.z;
+  base[(pp + 3) * N + n] = v.w;
+}
+__device__ __forceinline__ void store4(float* dst, float4 v) { *reinterpret_cast<float4*>(dst) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16* dst, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+
+// Outputs (carry-in states forward, dS backward) are written in the problem
+// dtype TOut; the scan itself runs in fp32.
+template <bool kBwd, typename TOut>
 __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs f) {
   __shared__ int s_ticket, s_flag;
   int* flags = kBwd ? f.flags_bwd : f.flags_fwd;
@@ -72,7 +99,7 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
   const int nk = min(kSpSeg, p.nc - k0);
   const float* achunk = f.achunk + bh * p.nc;
   const float* in = f.S;                 // forward: chunk states; backward: dHloc
-  float* out = kBwd ? f.S : f.Hin;       // forward: carry-in states; backward: dS (in place)
+  TOut* out = static_cast<TOut*>(kBwd ? f.dS : f.Hin);
   const size_t lb_slot = ((size_t)chain * p.sp_nseg + seg) * kSpElems + threadIdx.x * 4;
   const unsigned long long limit =
       (p.flags & SSD_TEST_DROP_SCAN_PUBLISH) ? kTestWaitLimitNs : kWaitLimitNs;
@@ -108,8 +135,7 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
   float4 prefix = make_float4(0.f, 0.f, 0.f, 0.f);
   if (seg == 0) {
     const float* start = kBwd ? f.dfinal : f.init;
-    if (start != nullptr && active)
-      prefix = *reinterpret_cast<const float4*>(start + bh * p.PN + e);
+    if (start != nullptr && active) prefix = load_public(start + bh * p.PN, e, p.P, p.N);
   } else {
     if (active) __stcg(reinterpret_cast<float4*>(f.agg + lb_slot), run);
     __threadfence();
@@ -163,7 +189,7 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
       if (sp < 0) {  // walked back to the chain start
         const float* start = kBwd ? f.dfinal : f.init;
         float4 sv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (start != nullptr && active) sv = *reinterpret_cast<const float4*>(start + bh * p.PN + e);
+        if (start != nullptr && active) sv = load_public(start + bh * p.PN, e, p.P, p.N);
         prefix = fma4(acc_a, sv, acc_v);
       } else {
         prefix = acc_v;  // timed out
@@ -185,13 +211,12 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
     for (int k = 0; k < kSpSeg; ++k) {
       if (k < nk) {
         const int c = kBwd ? p.nc - 1 - (k0 + k) : k0 + k;
-        *reinterpret_cast<float4*>(out + ((size_t)bh * p.nc + c) * p.PN + e) =
-            fma4(dprod[k], prefix, v[k]);
+        store4(out + ((size_t)bh * p.nc + c) * p.PN + e, fma4(dprod[k], prefix, v[k]));
       }
     }
     if (seg == p.sp_nseg - 1) {
       float* fin = kBwd ? f.dinit : f.final_states;
-      if (fin != nullptr) *reinterpret_cast<float4*>(fin + bh * p.PN + e) = incl;
+      if (fin != nullptr) store_public(fin + bh * p.PN, e, p.P, p.N, incl);
     }
   }
 }
@@ -200,10 +225,15 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
 
 cudaError_t launch_state_passing(const Plan& p, const Bufs& f, bool backward, cudaStream_t s) {
   const unsigned tiles = (unsigned)p.sp_chains * p.sp_nseg;
-  if (backward)
-    state_passing_kernel<true><<<tiles, kSpThreads, 0, s>>>(p, f);
+  set_kernel_name(backward ? "state_passing_bwd" : "state_passing_fwd");
+  if (backward && p.dtype == SSD_BF16)
+    state_passing_kernel<true, __nv_bfloat16><<<tiles, kSpThreads, 0, s>>>(p, f);
+  else if (backward)
+    state_passing_kernel<true, float><<<tiles, kSpThreads, 0, s>>>(p, f);
+  else if (p.dtype == SSD_BF16)
+    state_passing_kernel<false, __nv_bfloat16><<<tiles, kSpThreads, 0, s>>>(p, f);
   else
-    state_passing_kernel<false><<<tiles, kSpThreads, 0, s>>>(p, f);
+    state_passing_kernel<false, float><<<tiles, kSpThreads, 0, s>>>(p, f);
   return cudaGetLastError();
 }
 

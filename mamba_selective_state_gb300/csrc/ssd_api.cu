@@ -76,7 +76,9 @@ int make_plan(const ssd_problem* pr, Plan* p) {
   p->sp_neblk = (p->PN + kSpElems - 1) / kSpElems;
   p->sp_nseg = (p->nc + kSpSeg - 1) / kSpSeg;
   p->sp_chains = p->b * p->H * p->sp_neblk;
-  p->cb_ntb = (p->Q + 31) / 32;  // token blocks of 32 per chunk (chunk-backward kernel)
+  // per-chunk partial slots of the chunk-backward kernel: one per chunk on
+  // the tensor-core path, one per 32-token block on the CUDA-core path
+  p->cb_ntb = chunk_bwd_tc_supported(*p) ? 1 : (p->Q + 31) / 32;
 
   const size_t f4 = sizeof(float);
   const size_t bh = (size_t)p->b * p->H;
@@ -91,13 +93,14 @@ int make_plan(const ssd_problem* pr, Plan* p) {
   p->off_lcs = take(bh * p->Lp * f4);
   p->off_achunk = take(bh * p->nc * f4);
   p->off_S = take(states);
-  p->off_Hin = take(states);
+  p->off_Hin = take(states / 4 * (p->dtype == SSD_BF16 ? 2 : 4));
   const size_t lb = (size_t)p->sp_chains * p->sp_nseg;
   p->off_agg = take(lb * kSpElems * f4);
   p->off_incl = take(lb * kSpElems * f4);
   p->off_flags_fwd = take(lb * sizeof(int));
   p->off_flags_bwd = take(lb * sizeof(int));
   p->fwd_bytes = off;
+  p->off_dS = take(states / 4 * (p->dtype == SSD_BF16 ? 2 : 4));
   p->off_dl = take(bh * p->Lp * f4);
   p->off_ddte = take(bh * p->Lp * f4);
   p->off_udu = take(bh * p->nc * p->cb_ntb * f4);
@@ -118,12 +121,13 @@ void bind_workspace(const Plan& p, void* ws, bool bwd, Bufs* f) {
   f->lcs = reinterpret_cast<float*>(w + p.off_lcs);
   f->achunk = reinterpret_cast<float*>(w + p.off_achunk);
   f->S = reinterpret_cast<float*>(w + p.off_S);
-  f->Hin = reinterpret_cast<float*>(w + p.off_Hin);
+  f->Hin = w + p.off_Hin;
   f->agg = reinterpret_cast<float*>(w + p.off_agg);
   f->incl = reinterpret_cast<float*>(w + p.off_incl);
   f->flags_fwd = reinterpret_cast<int*>(w + p.off_flags_fwd);
   f->flags_bwd = reinterpret_cast<int*>(w + p.off_flags_bwd);
   if (bwd) {
+    f->dS = w + p.off_dS;
     f->dl = reinterpret_cast<float*>(w + p.off_dl);
     f->ddte = reinterpret_cast<float*>(w + p.off_ddte);
     f->udu = reinterpret_cast<float*>(w + p.off_udu);
@@ -141,9 +145,11 @@ int check_device() {
   return SSD_OK;
 }
 
-#define SSD_LAUNCH(expr)                      \
-  do {                                        \
-    cudaError_t e_ = (expr);                  \
+#define SSD_LAUNCH(expr)                        \
+  do {                                          \
+    prof_before(s);                             \
+    cudaError_t e_ = (expr);                    \
+    prof_after(s);                              \
     if (e_ != cudaSuccess) return SSD_ERR_CUDA; \
   } while (0)
 

@@ -40,11 +40,14 @@ struct Plan {
   int cb_ntb;
   // workspace offsets in bytes (0 = absent)
   size_t off_dte, off_lcs, off_achunk;   // (b,H,Lp) f32, (b,H,Lp) f32, (b,H,nc) f32
-  size_t off_S;                          // (b,H,nc,P,N) f32: chunk states / dHloc / dS
-  size_t off_Hin;                        // (b,H,nc,P,N) f32: carry-in states
+  // Chunk-state tensors are stored (b, H, nc, N, P): for each state index n a
+  // row of headdim values (the public initial/final states are (b, H, P, N)).
+  size_t off_S;                          // (b,H,nc,N,P) f32: chunk states, then dHloc
+  size_t off_Hin;                        // (b,H,nc,N,P) dtype: carry-in states
   size_t off_agg, off_incl;              // (chains, nseg, kSpElems) f32 each
   size_t off_flags_fwd, off_flags_bwd;   // (chains, nseg) int32 each
   // backward only
+  size_t off_dS;                         // (b,H,nc,N,P) dtype: dL/dS_c
   size_t off_dl, off_ddte;               // (b,H,Lp) f32 each
   size_t off_udu;                        // (b,H,nc,cb_ntb) f32
   size_t off_da;                         // (b,H,nc) f32
@@ -67,6 +70,7 @@ struct Bufs {
   void* y;
   float* final_states;
   // backward
+  void* dS;  // storage dtype of the problem
   const void* dy;
   const float* dfinal;
   void* dx;
@@ -83,7 +87,7 @@ struct Bufs {
   float* lcs;
   float* achunk;
   float* S;
-  float* Hin;
+  void* Hin;  // storage dtype of the problem
   float* agg;
   float* incl;
   int* flags_fwd;
@@ -130,5 +134,20 @@ cudaError_t launch_dt_bwd(const Plan& p, const Bufs& f, cudaStream_t s);
 cudaError_t launch_param_reduce(const Plan& p, const Bufs& f, cudaStream_t s);
 
 int device_sm_count();
+
+// Tensor-core variants (bf16, headdim 64); the launchers above use them when
+// the problem is inside their supported set.
+bool chunk_state_tc_supported(const Plan& p);
+cudaError_t launch_chunk_state_tc(const Plan& p, const Bufs& f, bool dstates, cudaStream_t s);
+bool chunk_scan_tc_supported(const Plan& p);
+cudaError_t launch_chunk_scan_tc(const Plan& p, const Bufs& f, cudaStream_t s);
+bool chunk_bwd_tc_supported(const Plan& p);
+cudaError_t launch_chunk_bwd_tc(const Plan& p, const Bufs& f, cudaStream_t s);
+
+// Per-kernel timing hooks (ssd_profile.cu): each launcher names the kernel it
+// launches; the entry points bracket every launch with prof_before/after.
+void set_kernel_name(const char* name);
+void prof_before(cudaStream_t s);
+void prof_after(cudaStream_t s);
 
 }  // namespace ssd
