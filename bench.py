@@ -48,21 +48,25 @@ def kernel_model(cfg, dtype_bytes):
     T = b * L
     tokx = T * H * P * s          # one (b,L,H,P) tensor in dtype
     tokbc = T * G * N * s         # one (b,L,G,N) tensor in dtype
-    st32 = b * H * nc * P * N * 4  # one fp32 chunk-state tensor
+    st32 = b * H * nc * P * N * 4  # chunk states / dHloc (fp32)
+    stS = b * H * nc * P * N * s   # carry-in states / dS (dtype)
     per_tok = b * H * Lp * 4      # one fp32 per-token-per-head vector
     units = b * H * nc            # (row, head, chunk) tiles
     gunits = b * G * nc           # (row, group, chunk) tiles
     m = {}
     m["dt_cumsum"] = dict(bytes=T * H * s + 2 * per_tok, flops=0)
     m["chunk_state"] = dict(bytes=tokx + tokbc + 2 * per_tok + st32, flops=2 * units * Q * P * N)
-    m["state_passing_fwd"] = dict(bytes=2 * st32, flops=2 * units * P * N)
-    m["chunk_scan"] = dict(bytes=2 * tokx + 2 * tokbc + st32 + 2 * per_tok,
+    m["state_passing_fwd"] = dict(bytes=st32 + stS, flops=2 * units * P * N)
+    m["chunk_scan"] = dict(bytes=2 * tokx + 2 * tokbc + stS + 2 * per_tok,
                            flops=gunits * 2 * Q * Q * N + units * (2 * Q * Q * P + 2 * Q * N * P))
     m["chunk_dstate"] = dict(bytes=tokx + tokbc + per_tok + st32, flops=2 * units * Q * P * N)
-    m["state_passing_bwd"] = dict(bytes=2 * st32, flops=2 * units * P * N)
-    m["chunk_bwd"] = dict(bytes=3 * tokx + 4 * tokbc + 2 * st32 + 4 * per_tok,
-                          flops=gunits * 2 * Q * Q * N
-                          + units * (8 * Q * P * N + 4 * Q * Q * P + 4 * Q * Q * N))
+    m["state_passing_bwd"] = dict(bytes=st32 + stS, flops=2 * units * P * N)
+    # per-head token gradients (dx, ddt_eff, dl): x, dy, B, C, dS, H_in in; dx out
+    m["chunk_bwd"] = dict(bytes=3 * tokx + 2 * tokbc + 2 * stS + 4 * per_tok,
+                          flops=units * (8 * Q * P * N + 4 * Q * Q * P + 4 * Q * Q * N))
+    # group gradients dB, dC: x, dy, B, C, dS, H_in in; dB, dC out
+    m["chunk_bwd_dbc"] = dict(bytes=2 * tokx + 4 * tokbc + 2 * stS + 2 * per_tok,
+                              flops=units * (4 * Q * Q * P + 4 * Q * Q * N + 4 * Q * P * N))
     m["dt_bwd"] = dict(bytes=2 * T * H * s + 4 * per_tok, flops=0)
     m["param_reduce"] = dict(bytes=b * nc * H * 4 * 4, flops=0)
     # compulsory IO of the layer (fwd reads x dt B C, writes y; bwd reads x dt
