@@ -177,6 +177,10 @@ __global__ void __launch_bounds__(kThr) chunk_bwd_tc_kernel(Plan p, Bufs f,
     for (int I = nb - 1; I >= J; --I) {
       if (I * kRows >= len) continue;
       const bool diag = (I == J);
+      // every thread has finished its waits on both barriers' previous phases
+      // before thread 0 arms them again
+      tc_fence_before();
+      __syncthreads();
       if (tid == 0) {
         mbar_expect_tx(&bar[0], 2 * tok_bytes + 2 * c_bytes);
         tma_load_4d(sX, &tmX, &bar[0], 0, h, t0 + J * kRows, bi);
@@ -504,6 +508,8 @@ __global__ void __launch_bounds__(kThr) chunk_bwd_dbc_tc_kernel(Plan p, Bufs f,
     for (int J = 0; J <= TB; ++J) {
       const uint8_t* bJ = sBT;
       const uint8_t* xJ = sXT;
+      tc_fence_before();
+      __syncthreads();  // all threads are past their previous barrier waits
       if (J != TB) {
         if (tid == 0) {
           mbar_expect_tx(&bar[0], tok_bytes + c_bytes);
@@ -580,6 +586,8 @@ __global__ void __launch_bounds__(kThr) chunk_bwd_dbc_tc_kernel(Plan p, Bufs f,
       if (I * kRows >= len) continue;
       const uint8_t* cI = sCT;
       const uint8_t* yI = sYT;
+      tc_fence_before();
+      __syncthreads();  // all threads are past their previous barrier waits
       if (I != TB) {
         if (tid == 0) {
           mbar_expect_tx(&bar[0], tok_bytes + c_bytes);

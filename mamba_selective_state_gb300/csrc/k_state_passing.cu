@@ -151,8 +151,11 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
         int fl = ld_acquire(fp);
         if (fl == kFlagNone) {
           const unsigned long long t_start = global_ns();
+          const long long c_start = clock64();
+          unsigned polls = 0;
           while ((fl = ld_acquire(fp)) == kFlagNone) {
-            if (global_ns() - t_start > limit) {
+            if (global_ns() - t_start > limit || clock64() - c_start > 2 * (long long)limit ||
+                ++polls > (1u << 24)) {
               atomicOr(&f.hdr->status, kDevTimeout);
               fl = -1;
               break;

@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ssd.h"
+#include "ssd.h"  // include/ (on the include path)
 
 namespace ssd {
 

@@ -58,15 +58,17 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 // Bounded wait for phase `parity` of `bar`.  Returns false if it did not
-// complete within about one second; the caller records the error.
+// complete within 2^31 SM clock cycles (about one second) or 2^20 polls,
+// whichever comes first; the caller records the error.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
+  const long long c0 = clock64();
+  for (uint32_t outer = 0; outer < (1u << 14); ++outer) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > 1000000000ull) return false;
+    if (clock64() - c0 > (1ll << 31)) return false;
   }
+  return false;
 }
 
 // ---- TMA ------------------------------------------------------------------

@@ -117,3 +117,13 @@ def test_bwd_argument_errors(lib):
     assert rc == lib.SSD_ERR_INVALID_ARGUMENT
     rc = lib.ssd_bwd(p, *args, workspace_bytes=1024, stream=0, check=False)
     assert rc == lib.SSD_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_profile_queries_without_records(lib):
+    # nothing recorded yet: no kernels, and an out-of-range index is rejected
+    assert lib.LIB.ssd_profile_count() == 0
+    name = ctypes.c_char_p()
+    n = ctypes.c_int()
+    ms = ctypes.c_double()
+    rc = lib.LIB.ssd_profile_get(0, ctypes.byref(name), ctypes.byref(n), ctypes.byref(ms))
+    assert rc == lib.SSD_ERR_INVALID_ARGUMENT
