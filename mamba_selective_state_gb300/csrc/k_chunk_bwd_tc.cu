@@ -662,30 +662,26 @@ __global__ void __launch_bounds__(kThr) chunk_bwd_dbc_tc_kernel(Plan p, Bufs f,
     if (!wait_mma(&bar[1], ph_mma)) ok = false;
     __syncthreads();  // before the next head's loads overwrite x/dy/dS/H and lq/dq
   }
-  // ---- epilogue: rows of dB and dC for the own block
+  // ---- epilogue: rows of dB and dC for the own block.  tcgen05.ld is a
+  // warp-collective instruction: every lane executes it, only the stores are
+  // guarded by the ragged end.
   {
     const int t = own0 + tid;
-    if (t < len) {
-      __nv_bfloat16* dB = static_cast<__nv_bfloat16*>(f.dB);
-      __nv_bfloat16* dC = static_cast<__nv_bfloat16*>(f.dC);
-      const long long row = (((long long)bi * p.L + t0 + t) * p.G + g) * p.N;
-      for (int n0 = 0; n0 < p.N; n0 += 16) {
-        float vb[16], vc[16];
-        tmem_ld16(tmem_addr(tDB, wlane, n0), vb);
-        tmem_ld16(tmem_addr(tDC, wlane, n0), vc);
+    const bool v = t < len;
+    __nv_bfloat16* dB = static_cast<__nv_bfloat16*>(f.dB);
+    __nv_bfloat16* dC = static_cast<__nv_bfloat16*>(f.dC);
+    const long long row = (((long long)bi * p.L + t0 + t) * p.G + g) * p.N;
+    for (int n0 = 0; n0 < p.N; n0 += 16) {
+      float vb[16], vc[16];
+      tmem_ld16(tmem_addr(tDB, wlane, n0), vb);
+      tmem_ld16(tmem_addr(tDC, wlane, n0), vc);
+      if (v) {
         uint4* ob = reinterpret_cast<uint4*>(dB + row + n0);
         uint4* oc = reinterpret_cast<uint4*>(dC + row + n0);
         ob[0] = make_uint4(pack2(vb[0], vb[1]), pack2(vb[2], vb[3]), pack2(vb[4], vb[5]), pack2(vb[6], vb[7]));
         ob[1] = make_uint4(pack2(vb[8], vb[9]), pack2(vb[10], vb[11]), pack2(vb[12], vb[13]), pack2(vb[14], vb[15]));
         oc[0] = make_uint4(pack2(vc[0], vc[1]), pack2(vc[2], vc[3]), pack2(vc[4], vc[5]), pack2(vc[6], vc[7]));
         oc[1] = make_uint4(pack2(vc[8], vc[9]), pack2(vc[10], vc[11]), pack2(vc[12], vc[13]), pack2(vc[14], vc[15]));
-      }
-    } else {
-      // tcgen05.ld is warp-collective: lanes past the end still take part
-      for (int n0 = 0; n0 < p.N; n0 += 16) {
-        float vb[16];
-        tmem_ld16(tmem_addr(tDB, wlane, n0), vb);
-        tmem_ld16(tmem_addr(tDC, wlane, n0), vb);
       }
     }
   }
