@@ -8,7 +8,7 @@
 //   dx_j      = sum_i M_ij dy_i + u_j dS B_j + D_h dy_j
 //   ddt_eff_j = sum_i dM_ij (C_i.B_j) E_ij + sv_j exp(l_last - l_j) (x_j . dS B_j)
 //   dl_t      = sum_j R_tj - sum_i R_it + [cv_t] e^{l_t} dy_t . (H C_t) - u_t (x_t . dS B_t)
-// and the per-chunk partials sum_j u_j (x_j . dS B_j), <dS, H>, sum dy . x.
+// and the per-chunk partials sum_j u_j (x_j . dS B_j) and sum dy . x.
 //
 // One CTA (256 threads) per (row, chunk, group).  C B^T does not depend on the
 // head: it is formed once and stays in tensor memory.  For each head of the
@@ -252,28 +252,8 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_group_tc_kernel(Plan p, Buf
     }
     __syncthreads();  // lq/dq of this head visible
     if (!wait_mma(&bar[4], ph_m1)) ok = false;
-    // <dS, H> of this head (before the next head's state tiles arrive)
-    float da_part = 0.0f;
-    if (tid < p.N) {
-      for (int q = 0; q < 8; ++q) {
-        const uint4 a = *reinterpret_cast<const uint4*>(sS + swz128_off(tid, q * 8));
-        const uint4 b = *reinterpret_cast<const uint4*>(sH + swz128_off(tid, q * 8));
-        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 x2 = unpack2(av[e]), y2 = unpack2(bv[e]);
-          da_part += x2.x * y2.x + x2.y * y2.y;
-        }
-      }
-    }
-    if (tid < kRows) red[tid] = da_part;
-    __syncthreads();  // dS, H consumed (MMAs done, da read): prefetch the next head
-    if (tid == 0) {
-      if (hh + 1 < hpg) issue_sh(hh + 1);
-      float sa = 0.0f;
-      for (int t = 0; t < kRows; ++t) sa += red[t];
-      f.da[bh * p.nc + c] = sa;
-    }
+    __syncthreads();  // dS, H consumed by the finished MMAs: prefetch the next head's
+    if (tid == 0 && hh + 1 < hpg) issue_sh(hh + 1);
     // ---- mask pass: thread row i, column half wg
     {
       const float li = tok_ok ? lq[i] : 0.0f;

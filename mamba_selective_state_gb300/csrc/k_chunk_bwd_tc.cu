@@ -10,7 +10,7 @@
 //   dx_j      = sum_{i>=j} M_ij dy_i + u_j dS B_j + D_h dy_j
 //   ddt_eff_j = sum_{i>=j} dM_ij (C_i.B_j) E_ij + sv_j exp(l_last-l_j) (x_j.dS B_j)
 //   dl_t      = sum_j dM_tj M_tj - sum_i dM_it M_it + [cv_t] e^{l_t} dy_t.(H C_t) - u_t (x_t.dS B_t)
-// and per-chunk partials sum_j u_j (x_j.dS B_j), <dS, H>, sum dy.x.  Every
+// and per-chunk partials sum_j u_j (x_j.dS B_j), sum dy.x.  Every
 // 128 x 128 token tile is formed in both orientations on the tensor cores
 // (C B^T and B C^T, dy x^T and x dy^T), so each row sum and each column sum
 // is taken by the thread that owns that token, in fp32 and in a fixed order.
@@ -350,38 +350,21 @@ __global__ void __launch_bounds__(kThr) chunk_bwd_tc_kernel(Plan p, Bufs f,
       }
     }
   }
-  // dL/da_c = <dS, H> over the (N x 64) state tiles
-  float da_part = 0.0f;
-  if (tid < p.N) {
-    for (int q = 0; q < 8; ++q) {
-      const uint4 a = *reinterpret_cast<const uint4*>(sS + swz128_off(tid, q * 8));
-      const uint4 b = *reinterpret_cast<const uint4*>(sH + swz128_off(tid, q * 8));
-      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 x = unpack2(av[e]), y = unpack2(bv[e]);
-        da_part += x.x * y.x + x.y * y.y;
-      }
-    }
-  }
   red[tid] = udu_part;
   red[kThr + tid] = dD_part;
-  red[2 * kThr + tid] = da_part;
   __syncthreads();
   for (int t = tid; t < len; t += kThr) {
     f.ddte[bh * p.Lp + t0 + t] = dda[t];
     f.dl[bh * p.Lp + t0 + t] = dla[t];
   }
   if (tid == 0) {
-    float su = 0.0f, sd = 0.0f, sa = 0.0f;
+    float su = 0.0f, sd = 0.0f;
     for (int t = 0; t < kThr; ++t) {
       su += red[t];
       sd += red[kThr + t];
-      sa += red[2 * kThr + t];
     }
     f.udu[bh * p.nc + c] = su;
     f.pdD[((long long)bi * p.nc + c) * p.H + h] = sd;
-    f.da[bh * p.nc + c] = sa;
   }
   if (!ok) atomicOr(&f.hdr->status, kDevTimeout);
   tc_fence_before();

@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_simt(Plan p, Bufs f) {
     }
     __syncthreads();
   }
-  float* out = f.S + (bh * p.nc + c) * p.PN;
+  float* out = (kDstates ? f.dHl : f.S) + (bh * p.nc + c) * p.PN;
 #pragma unroll
   for (int k = 0; k < kMaxOut; ++k)
     if (k < nout) out[threadIdx.x + k * kThreads] = acc[k];
@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_simt(Plan p, Bufs f) {
 //     dB_j += sum_i dM_ij E_ij dt_eff_j C_i;  ddt_eff_j += sum_i dM_ij (C_i.B_j) E_ij;
 //     dl_i += sum_j dM_ij M_ij;  dl_j -= sum_i dM_ij M_ij
 //   skip part: dx_j += D_h dy_j;  dD_h += dy_j . x_j
-// The dl_last terms (sum over the chunk, and a_c dL/da_c with
-// dL/da_c = <dS, H_in[c]>) go to per-block partials folded by dt_bwd.
+// The dl_last term summed over the chunk goes to per-block partials folded by
+// dt_bwd (the other dl_last term, a_c dL/da_c, comes from the reverse scan).
 template <typename T>
 __global__ void __launch_bounds__(kThreads) chunk_bwd_simt(Plan p, Bufs f) {
   extern __shared__ float smem[];
@@ -499,21 +499,6 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt(Plan p, Bufs f) {
       }
       f.pdD[(((long long)bi * p.nc + c) * ntb + tb) * p.H + h] = sd;
       f.udu[(bh * p.nc + c) * ntb + tb] = su;
-    }
-    if (tb == 0) {  // dL/da_c = <dS, H_in[c]>, folded in a fixed order
-      float s = 0.0f;
-      for (int idx = threadIdx.x; idx < p.PN; idx += kThreads) {
-        const int n = idx / P, pp = idx - n * P;
-        s = fmaf(dSs[pp * N1 + n], Hs[pp * N1 + n], s);
-      }
-      __syncthreads();
-      red[threadIdx.x] = s;
-      __syncthreads();
-      for (int st = kThreads / 2; st > 0; st >>= 1) {
-        if (threadIdx.x < st) red[threadIdx.x] += red[threadIdx.x + st];
-        __syncthreads();
-      }
-      if (threadIdx.x == 0) f.da[bh * p.nc + c] = red[0];
     }
   }
   __syncthreads();

@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(Plan p, Bufs f,
     const int wq = tid >> 5, lane = tid & 31;
     const int m = wq * 32 + lane;
     const long long bh = (long long)bi * p.H + h0 + (m >> 6);
-    float* out = f.S + (bh * p.nc + c) * p.PN + (m & 63);
+    float* out = (kDstates ? f.dHl : f.S) + (bh * p.nc + c) * p.PN + (m & 63);
     for (int n0 = 0; n0 < p.N; n0 += 16) {
       float v[16];
       tmem_ld16(tmem_addr(tmem, wq * 32, n0), v);

@@ -113,7 +113,12 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Plan p, Bufs f) {
     const float* u = f.udu + (bh * p.nc + c) * p.cb_ntb;
     for (int tb = 0; tb < p.cb_ntb; ++tb) extra += u[tb];
     const float a = f.achunk[bh * p.nc + c];
-    if (a != 0.0f) extra += a * f.da[bh * p.nc + c];
+    if (a != 0.0f) {
+      float da = 0.0f;
+      const float* dp = f.dapart + (bh * p.nc + c) * p.sp_neblk;
+      for (int k = 0; k < p.sp_neblk; ++k) da += dp[k];
+      extra += a * da;
+    }
   }
   extra = __shfl_sync(kFull, extra, 0);
   float dl[kMaxPerLane];

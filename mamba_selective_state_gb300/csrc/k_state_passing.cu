@@ -82,9 +82,15 @@ __device__ __forceinline__ void store4(__nv_bfloat16* dst, float4 v) {
 
 // Outputs (carry-in states forward, dS backward) are written in the problem
 // dtype TOut; the scan itself runs in fp32.
-template <bool kBwd, typename TOut>
+// kKeepF32 (forward only): also store the fp32 carry-in states over the chunk
+// states just read (each element is read before it is written, by the same
+// thread).  The backward also forms dL/da_c = <dS_c, H_in[c]> in fp32 from
+// those fp32 carry-in states: one partial per (chunk, element block), folded
+// over the block's warps in a fixed order.
+template <bool kBwd, bool kKeepF32, typename TOut>
 __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs f) {
   __shared__ int s_ticket, s_flag;
+  __shared__ float s_da[kSpSeg][kSpThreads / 32];
   int* flags = kBwd ? f.flags_bwd : f.flags_fwd;
   if (threadIdx.x == 0) s_ticket = atomicAdd(kBwd ? &f.hdr->ticket_bwd : &f.hdr->ticket_fwd, 1);
   __syncthreads();
@@ -98,7 +104,7 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
   const int k0 = seg * kSpSeg;
   const int nk = min(kSpSeg, p.nc - k0);
   const float* achunk = f.achunk + bh * p.nc;
-  const float* in = f.S;                 // forward: chunk states; backward: dHloc
+  const float* in = kBwd ? f.dHl : f.S;  // forward: chunk states; backward: dHloc
   TOut* out = static_cast<TOut*>(kBwd ? f.dS : f.Hin);
   const size_t lb_slot = ((size_t)chain * p.sp_nseg + seg) * kSpElems + threadIdx.x * 4;
   const unsigned long long limit =
@@ -209,14 +215,39 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
   }
 
   // 3) carry-in values of the segment's chunks, and the end of the chain
-  if (active) {
 #pragma unroll
-    for (int k = 0; k < kSpSeg; ++k) {
-      if (k < nk) {
-        const int c = kBwd ? p.nc - 1 - (k0 + k) : k0 + k;
-        store4(out + ((size_t)bh * p.nc + c) * p.PN + e, fma4(dprod[k], prefix, v[k]));
+  for (int k = 0; k < kSpSeg; ++k) {
+    if (k < nk) {
+      const int c = kBwd ? p.nc - 1 - (k0 + k) : k0 + k;
+      const size_t off = ((size_t)bh * p.nc + c) * p.PN + e;
+      const float4 val = fma4(dprod[k], prefix, v[k]);
+      if (active) {
+        store4(out + off, val);
+        if (kKeepF32) *reinterpret_cast<float4*>(f.S + off) = val;
+      }
+      if (kBwd) {
+        float d = 0.0f;
+        if (active) {
+          const float4 hv = __ldcs(reinterpret_cast<const float4*>(f.S + off));
+          d = val.x * hv.x + val.y * hv.y + val.z * hv.z + val.w * hv.w;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        if ((threadIdx.x & 31) == 0) s_da[k][threadIdx.x >> 5] = d;
       }
     }
+  }
+  if (kBwd) {
+    __syncthreads();
+    if (threadIdx.x < nk) {
+      const int k = threadIdx.x;
+      const int c = p.nc - 1 - (k0 + k);
+      float d = 0.0f;
+      for (int w = 0; w < kSpThreads / 32; ++w) d += s_da[k][w];
+      f.dapart[((size_t)bh * p.nc + c) * p.sp_neblk + eblk] = d;
+    }
+  }
+  if (active) {
     if (seg == p.sp_nseg - 1) {
       float* fin = kBwd ? f.dinit : f.final_states;
       if (fin != nullptr) store_public(fin + bh * p.PN, e, p.P, p.N, incl);
@@ -226,17 +257,20 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
 
 }  // namespace
 
-cudaError_t launch_state_passing(const Plan& p, const Bufs& f, bool backward, cudaStream_t s) {
+cudaError_t launch_state_passing(const Plan& p, const Bufs& f, bool backward, bool keep_f32, cudaStream_t s) {
   const unsigned tiles = (unsigned)p.sp_chains * p.sp_nseg;
   set_kernel_name(backward ? "state_passing_bwd" : "state_passing_fwd");
-  if (backward && p.dtype == SSD_BF16)
-    state_passing_kernel<true, __nv_bfloat16><<<tiles, kSpThreads, 0, s>>>(p, f);
-  else if (backward)
-    state_passing_kernel<true, float><<<tiles, kSpThreads, 0, s>>>(p, f);
-  else if (p.dtype == SSD_BF16)
-    state_passing_kernel<false, __nv_bfloat16><<<tiles, kSpThreads, 0, s>>>(p, f);
-  else
-    state_passing_kernel<false, float><<<tiles, kSpThreads, 0, s>>>(p, f);
+  const bool bf = p.dtype == SSD_BF16;
+  if (backward) {
+    if (bf) state_passing_kernel<true, false, __nv_bfloat16><<<tiles, kSpThreads, 0, s>>>(p, f);
+    else state_passing_kernel<true, false, float><<<tiles, kSpThreads, 0, s>>>(p, f);
+  } else if (keep_f32) {
+    if (bf) state_passing_kernel<false, true, __nv_bfloat16><<<tiles, kSpThreads, 0, s>>>(p, f);
+    else state_passing_kernel<false, true, float><<<tiles, kSpThreads, 0, s>>>(p, f);
+  } else {
+    if (bf) state_passing_kernel<false, false, __nv_bfloat16><<<tiles, kSpThreads, 0, s>>>(p, f);
+    else state_passing_kernel<false, false, float><<<tiles, kSpThreads, 0, s>>>(p, f);
+  }
   return cudaGetLastError();
 }
 

@@ -101,10 +101,11 @@ int make_plan(const ssd_problem* pr, Plan* p) {
   p->off_flags_bwd = take(lb * sizeof(int));
   p->fwd_bytes = off;
   p->off_dS = take(states / 4 * (p->dtype == SSD_BF16 ? 2 : 4));
+  p->off_dHl = take(states);
+  p->off_dapart = take(bh * p->nc * p->sp_neblk * f4);
   p->off_dl = take(bh * p->Lp * f4);
   p->off_ddte = take(bh * p->Lp * f4);
   p->off_udu = take(bh * p->nc * p->cb_ntb * f4);
-  p->off_da = take(bh * p->nc * f4);
   p->off_pdA = take(bh * p->nc * f4);
   p->off_pdb = take(bh * p->nc * f4);
   p->off_pdD = take(bh * p->nc * p->cb_ntb * f4);
@@ -131,7 +132,8 @@ void bind_workspace(const Plan& p, void* ws, bool bwd, Bufs* f) {
     f->dl = reinterpret_cast<float*>(w + p.off_dl);
     f->ddte = reinterpret_cast<float*>(w + p.off_ddte);
     f->udu = reinterpret_cast<float*>(w + p.off_udu);
-    f->da = reinterpret_cast<float*>(w + p.off_da);
+    f->dHl = reinterpret_cast<float*>(w + p.off_dHl);
+    f->dapart = reinterpret_cast<float*>(w + p.off_dapart);
     f->pdA = reinterpret_cast<float*>(w + p.off_pdA);
     f->pdb = reinterpret_cast<float*>(w + p.off_pdb);
     f->pdD = reinterpret_cast<float*>(w + p.off_pdD);
@@ -203,7 +205,7 @@ int ssd_fwd(const ssd_problem* prob, const void* x, const void* dt, const float*
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   SSD_LAUNCH(launch_dt_cumsum(p, f, s));
   SSD_LAUNCH(launch_chunk_state(p, f, false, s));
-  SSD_LAUNCH(launch_state_passing(p, f, false, s));
+  SSD_LAUNCH(launch_state_passing(p, f, false, false, s));
   SSD_LAUNCH(launch_chunk_scan(p, f, s));
   return SSD_OK;
 }
@@ -244,10 +246,10 @@ int ssd_bwd(const ssd_problem* prob, const void* x, const void* dt, const float*
   // recompute the forward intermediates: dt_eff, chunk cumsums, carry-in states
   SSD_LAUNCH(launch_dt_cumsum(p, f, s));
   SSD_LAUNCH(launch_chunk_state(p, f, false, s));
-  SSD_LAUNCH(launch_state_passing(p, f, false, s));
+  SSD_LAUNCH(launch_state_passing(p, f, false, true, s));
   // gradient of the carry-in states from y, then the reverse state-passing scan
   SSD_LAUNCH(launch_chunk_state(p, f, true, s));
-  SSD_LAUNCH(launch_state_passing(p, f, true, s));
+  SSD_LAUNCH(launch_state_passing(p, f, true, false, s));
   SSD_LAUNCH(launch_chunk_bwd(p, f, s));
   SSD_LAUNCH(launch_dt_bwd(p, f, s));
   SSD_LAUNCH(launch_param_reduce(p, f, s));

@@ -42,15 +42,17 @@ struct Plan {
   size_t off_dte, off_lcs, off_achunk;   // (b,H,Lp) f32, (b,H,Lp) f32, (b,H,nc) f32
   // Chunk-state tensors are stored (b, H, nc, N, P): for each state index n a
   // row of headdim values (the public initial/final states are (b, H, P, N)).
-  size_t off_S;                          // (b,H,nc,N,P) f32: chunk states, then dHloc
+  size_t off_S;                          // (b,H,nc,N,P) f32: chunk states; in the backward,
+                                         // then the fp32 carry-in states (in place)
   size_t off_Hin;                        // (b,H,nc,N,P) dtype: carry-in states
   size_t off_agg, off_incl;              // (chains, nseg, kSpElems) f32 each
   size_t off_flags_fwd, off_flags_bwd;   // (chains, nseg) int32 each
   // backward only
   size_t off_dS;                         // (b,H,nc,N,P) dtype: dL/dS_c
+  size_t off_dHl;                        // (b,H,nc,N,P) f32: dL/dH_in[c] from the chunk outputs
+  size_t off_dapart;                     // (b,H,nc,neblk) f32: partial sums of dL/da_c
   size_t off_dl, off_ddte;               // (b,H,Lp) f32 each
   size_t off_udu;                        // (b,H,nc,cb_ntb) f32
-  size_t off_da;                         // (b,H,nc) f32
   size_t off_pdA, off_pdb;               // (b,nc,H) f32 partials of dA, ddt_bias
   size_t off_pdD;                        // (b,nc,cb_ntb,H) f32 partials of dD
   size_t fwd_bytes, bwd_bytes;
@@ -95,7 +97,8 @@ struct Bufs {
   float* dl;
   float* ddte;
   float* udu;
-  float* da;
+  float* dHl;
+  float* dapart;
   float* pdA;
   float* pdb;
   float* pdD;
@@ -126,7 +129,9 @@ __device__ __forceinline__ int seg_in_of(const Plan& p, const Bufs& f, int bi, i
 
 // Host launchers (each returns the launch's cudaError_t).
 cudaError_t launch_dt_cumsum(const Plan& p, const Bufs& f, cudaStream_t s);
-cudaError_t launch_state_passing(const Plan& p, const Bufs& f, bool backward, cudaStream_t s);
+// backward: the reverse scan (dS, dinit, dL/da_c partials); keep_f32 (forward
+// only): also keep the fp32 carry-in states, in place over the chunk states.
+cudaError_t launch_state_passing(const Plan& p, const Bufs& f, bool backward, bool keep_f32, cudaStream_t s);
 cudaError_t launch_chunk_state(const Plan& p, const Bufs& f, bool dstates, cudaStream_t s);
 cudaError_t launch_chunk_scan(const Plan& p, const Bufs& f, cudaStream_t s);
 cudaError_t launch_chunk_bwd(const Plan& p, const Bufs& f, cudaStream_t s);
