@@ -133,6 +133,28 @@ const char* ssd_status_string(int status);
  * the synchronisation or the copy fails. */
 int ssd_read_device_status(const void* workspace, ssd_stream_t stream);
 
+/* Allocation-free forward.  The pages have no counterpart: this is a
+ * library convenience for callers that cannot allocate device memory where
+ * they call the layer -- a plain C host with no handle on the framework's
+ * caching allocator, or a latency-critical loop where an allocation (and
+ * the synchronisation cudaMalloc implies) is not allowed.  Same arguments
+ * and results as ssd_fwd, minus the workspace: the workspace is a
+ * library-owned device array of SSD_NOALLOC_SCRATCH_BYTES (32 MiB) that
+ * every GPU loading libssd holds until the process exits.  Problems whose
+ * ssd_fwd_workspace_bytes exceeds it are rejected with
+ * SSD_ERR_WORKSPACE_TOO_SMALL.  The call allocates nothing.  Its first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current) and caches it; make that first call before any
+ * stream capture.  All calls share the one array and it keeps the last
+ * call's contents (each call re-zeroes what must start at zero): calls that
+ * can overlap on the GPU -- on different streams or from different host
+ * threads -- race on it. */
+#define SSD_NOALLOC_SCRATCH_BYTES (32u << 20)
+int ssd_fwd_noalloc(const ssd_problem* prob, const void* x, const void* dt, const float* dt_bias,
+                    const float* A, const void* B, const void* C, const float* D,
+                    const float* initial_states, const int32_t* seq_idx, void* y,
+                    float* final_states, ssd_stream_t stream);
+
 /* Library build/version string, e.g. "libssd 0.1 sm_103a". */
 const char* ssd_version(void);
 

@@ -30,7 +30,8 @@ SSD_TEST_DROP_SCAN_PUBLISH = 1 << 16
 # every symbol include/ssd.h declares
 EXPORTS = ["ssd_fwd_workspace_bytes", "ssd_bwd_workspace_bytes", "ssd_fwd", "ssd_bwd",
            "ssd_status_string", "ssd_read_device_status", "ssd_version", "ssd_profile_start",
-           "ssd_profile_stop", "ssd_profile_count", "ssd_profile_get"]
+           "ssd_profile_stop", "ssd_profile_count", "ssd_profile_get", "ssd_fwd_noalloc"]
+SSD_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class ssd_problem(ctypes.Structure):
@@ -73,6 +74,8 @@ def _load():
     lib.ssd_profile_get.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p),
                                     ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)]
     lib.ssd_profile_get.restype = i32
+    lib.ssd_fwd_noalloc.argtypes = [pp] + [vp] * 11 + [vp]
+    lib.ssd_fwd_noalloc.restype = i32
     return lib
 
 
@@ -170,3 +173,12 @@ def profile_stop() -> dict:
     if rc == SSD_ERR_WORKSPACE_TOO_SMALL:
         out["_dropped"] = (1, 0.0)
     return out
+
+
+def ssd_fwd_noalloc(prob, x, dt, dt_bias, A, B, C, D, initial_states, seq_idx, y, final_states,
+                    stream=None) -> int:
+    """Forward with the library-owned workspace (no workspace argument, no
+    allocation); returns the status code."""
+    return int(LIB.ssd_fwd_noalloc(ctypes.byref(prob), _p(x), _p(dt), _p(dt_bias), _p(A), _p(B),
+                                   _p(C), _p(D), _p(initial_states), _p(seq_idx), _p(y),
+                                   _p(final_states), _stream(stream)))
