@@ -57,10 +57,13 @@ def kernel_model(cfg, dtype_bytes):
     m["dt_cumsum"] = dict(bytes=T * H * s + 2 * per_tok, flops=0)
     m["chunk_state"] = dict(bytes=tokx + tokbc + 2 * per_tok + st32, flops=2 * units * Q * P * N)
     m["state_passing_fwd"] = dict(bytes=st32 + stS, flops=2 * units * P * N)
+    # the backward's forward pass also keeps the fp32 carry-in states (in place)
+    m["state_passing_fwd_keep"] = dict(bytes=2 * st32 + stS, flops=2 * units * P * N)
     m["chunk_scan"] = dict(bytes=2 * tokx + 2 * tokbc + stS + 2 * per_tok,
                            flops=gunits * 2 * Q * Q * N + units * (2 * Q * Q * P + 2 * Q * N * P))
     m["chunk_dstate"] = dict(bytes=tokx + tokbc + per_tok + st32, flops=2 * units * Q * P * N)
-    m["state_passing_bwd"] = dict(bytes=st32 + stS, flops=2 * units * P * N)
+    # reads dHloc and the fp32 carry-in states (for dL/da_c), writes dS
+    m["state_passing_bwd"] = dict(bytes=2 * st32 + stS, flops=4 * units * P * N)
     # per-head token gradients (dx, ddt_eff, dl): x, dy, B, C, dS, H_in in; dx out
     m["chunk_bwd"] = dict(bytes=3 * tokx + 2 * tokbc + 2 * stS + 4 * per_tok,
                           flops=units * (8 * Q * P * N + 4 * Q * Q * P + 4 * Q * Q * N))

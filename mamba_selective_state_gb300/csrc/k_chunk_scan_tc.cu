@@ -12,13 +12,16 @@
 // the tensor cores (M = 128 rows, N = 128 tokens per column block J <= the
 // row block, K = d_state) and stays in tensor memory.  The heads are then
 // streamed: their x and carry-in-state tiles arrive by TMA into a double
-// buffer while the previous head is processed; eight warps read C B^T back
-// (one TMEM lane = one row; the two warpgroups split the columns), apply the
+// buffer while the previous head is processed; sixteen warps read C B^T back
+// (one TMEM lane = one row; the four warpgroups split the columns), apply the
 // causal / same-sequence mask, exp(l_i - l_j) and dt_eff_j of the head, and
 // write the bf16 K-major A_hat tile; one thread issues Y1 = A_hat X and the
 // carry Y2 = C H_in^T into a double-buffered accumulator pair, and the
 // epilogue y = Y1 + cv e^{l} Y2 + D x of head h-1 runs while the tensor core
-// works on head h.
+// works on head h.  Per-head l and dt_eff are prefetched two heads ahead
+// into a ring of three shared-memory slots, the epilogue's x row one head
+// ahead into registers, and 16-column blocks wholly above the diagonal for a
+// warp's 32 rows are written as zeros without reading tensor memory.
 #include "ssd_internal.cuh"
 #include "tc_common.cuh"
 #include "tma_host.h"
@@ -30,7 +33,7 @@ namespace {
 using namespace tc;
 
 constexpr int kRows = 128;  // rows (tokens i) per CTA = MMA M
-constexpr int kThr = 256;   // two warpgroups
+constexpr int kThr = 512;   // four warpgroups: four warps per quarter of the TMEM lanes
 
 __host__ __device__ inline uint32_t r1024(uint32_t v) { return (v + 1023u) & ~1023u; }
 
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_scan_tc_kernel(Plan p, Bufs f,
   const int I = blockIdx.x % G.nJ, c = blockIdx.x / G.nJ;
   const int g = blockIdx.y, bi = blockIdx.z;
   const int tid = threadIdx.x;
-  const int wg = tid >> 7;          // warpgroup: column half of the mask pass
+  const int wg = tid >> 7;          // warpgroup: column quarter of the mask pass
   const int ri = tid & 127;         // row (TMEM lane) of this thread
   const int wlane = ((tid >> 5) & 3) * 32;
   const int t0 = c * p.Q, len = min(p.Q, p.L - t0);
@@ -94,13 +97,20 @@ __global__ void __launch_bounds__(kThr, 1) chunk_scan_tc_kernel(Plan p, Bufs f,
   uint8_t* sX = sm + G.offX;
   uint8_t* sH = sm + G.offH;
   const uint32_t hbytes = r1024((uint32_t)p.N * 128u);
-  float* lq = reinterpret_cast<float*>(sm + G.offF);   // [2][Q] per-buffer head scalars
-  float* dq = lq + 2 * p.Q;                            // [2][Q]
-  int* sq = reinterpret_cast<int*>(dq + 2 * p.Q);      // [Q]
+  float* lq = reinterpret_cast<float*>(sm + G.offF);   // [3][Q] head scalars, ring of 3 heads
+  float* dq = lq + 3 * p.Q;                            // [3][Q]
+  int* sq = reinterpret_cast<int*>(dq + 3 * p.Q);      // [Q]
   uint64_t* bar = reinterpret_cast<uint64_t*>(sq + p.Q);  // ld[2], mma[2], cb
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 5);
 
   for (int t = tid; t < p.Q; t += kThr) sq[t] = t < len ? seg_of(p, f, bi, (long long)t0 + t) : -1;
+  for (int k = 0; k < 2 && k < p.hpg; ++k) {  // scalars of the first two heads
+    const long long bhk = (long long)bi * p.H + g * p.hpg + k;
+    for (int t = tid; t < p.Q; t += kThr) {
+      lq[k * p.Q + t] = f.lcs[bhk * p.Lp + t0 + t];
+      dq[k * p.Q + t] = f.dte[bhk * p.Lp + t0 + t];
+    }
+  }
   if (G.rows < kRows)  // K padding rows of the x tiles must be zero
     for (int idx = tid; idx < 2 * (kRows - G.rows) * 8; idx += kThr) {
       const int buf = idx / ((kRows - G.rows) * 8), k = idx % ((kRows - G.rows) * 8);
@@ -169,21 +179,28 @@ __global__ void __launch_bounds__(kThr, 1) chunk_scan_tc_kernel(Plan p, Bufs f,
   __nv_bfloat16* y = static_cast<__nv_bfloat16*>(f.y);
   const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(f.x);
 
-  auto epilogue = [&](int hh) {  // y rows of head hh from accumulator buffer hh&1
+  // x row of head hh for the skip term (this thread's row, its 32 columns),
+  // fetched one iteration ahead of its use
+  auto fetch_x = [&](int hh, uint4 (&xv)[2]) {
+    const long long xrow = (((long long)bi * p.L + t0 + i) * p.H + h_first + hh) * 64 + wg * 16;
+    const uint4* xr = reinterpret_cast<const uint4*>(xg + xrow);
+    xv[0] = row_ok ? xr[0] : make_uint4(0, 0, 0, 0);
+    xv[1] = row_ok ? xr[1] : make_uint4(0, 0, 0, 0);
+  };
+  // y rows of head hh from accumulator buffer hh&1; li is the row's l of head
+  // hh, kept in a register from the mask pass (its ring slot is refilled in
+  // the same iteration as this epilogue runs)
+  auto epilogue = [&](int hh, const uint4 (&xv)[2], float li) {
     const int buf = hh & 1, h = h_first + hh;
-    const long long bh = (long long)bi * p.H + h;
-    const float li = row_ok ? f.lcs[bh * p.Lp + t0 + i] : 0.0f;
     const float carry = (row_ok && si == s_in) ? __expf(li) : 0.0f;
     const float Dh = f.D[h];
     const long long yrow = (((long long)bi * p.L + t0 + i) * p.H + h) * 64;
-    const int q0 = wg * 2;  // the two warpgroups split the 64 output columns
-    for (int q = q0; q < q0 + 2; ++q) {
+    {
+      const int q = wg;  // the four warpgroups split the 64 output columns
       float a[16], b[16];
-      tmem_ld16(tmem_addr(tY + buf * 128, wlane, q * 16), a);
-      tmem_ld16(tmem_addr(tY + buf * 128 + 64, wlane, q * 16), b);
+      tmem_ld16x2(tmem_addr(tY + buf * 128, wlane, q * 16), tmem_addr(tY + buf * 128 + 64, wlane, q * 16), a, b);
       if (row_ok) {
-        const uint4* xr = reinterpret_cast<const uint4*>(xg + yrow + q * 16);
-        const uint4 x0 = xr[0], x1 = xr[1];
+        const uint4 x0 = xv[0], x1 = xv[1];
         const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         uint32_t o[8];
 #pragma unroll
@@ -199,14 +216,21 @@ __global__ void __launch_bounds__(kThr, 1) chunk_scan_tc_kernel(Plan p, Bufs f,
     }
   };
 
+  uint4 xprev[2] = {};
+  float li_prev = 0.0f;  // l of the head whose epilogue is pending
   for (int hh = 0; hh < hpg; ++hh) {
-    const int buf = hh & 1, h = h_first + hh;
-    const long long bh = (long long)bi * p.H + h;
-    // head scalars into this buffer's slots (their previous reader, the mask
-    // pass of head hh-2, finished before the barrier that ended iteration hh-1)
-    for (int t = tid; t < p.Q; t += kThr) {
-      lq[buf * p.Q + t] = f.lcs[bh * p.Lp + t0 + t];
-      dq[buf * p.Q + t] = f.dte[bh * p.Lp + t0 + t];
+    const int buf = hh & 1;
+    // prefetch, for later in this iteration: the x row of head hh-1 (epilogue)
+    // and the scalars of head hh+2 (ring slot (hh+2)%3, last read by head hh-1)
+    uint4 xcur[2];
+    if (hh > 0) fetch_x(hh - 1, xcur);
+    const int pre = hh + 2;
+    float pl = 0.0f, pd = 0.0f;
+    const int tq = tid;  // Q <= 256 < kThr: one scalar pair per thread
+    if (pre < hpg && tq < p.Q) {
+      const long long bhp = (long long)bi * p.H + h_first + pre;
+      pl = f.lcs[bhp * p.Lp + t0 + tq];
+      pd = f.dte[bhp * p.Lp + t0 + tq];
     }
     if (hh > 0) {  // MMAs of head hh-1 done: A_hat and the other buffers are free
       if (!mbar_wait(&bar[2 + ((hh - 1) & 1)], ((hh - 1) >> 1) & 1)) ok = false;
@@ -215,24 +239,27 @@ __global__ void __launch_bounds__(kThr, 1) chunk_scan_tc_kernel(Plan p, Bufs f,
     }
     __syncthreads();
     {  // mask pass: row ri, column half wg of every block J
-      const float* lb = lq + buf * p.Q;
-      const float* db = dq + buf * p.Q;
+      const float* lb = lq + (hh % 3) * p.Q;
+      const float* db = dq + (hh % 3) * p.Q;
       const float li = row_ok ? lb[i] : 0.0f;
+      const int warp_last_row = i0 + wlane + 31;  // last row of this warp
       for (int J = 0; J < nJ; ++J) {
         uint8_t* aJ = sB + J * bsp;
-        for (int q = wg * 4; q < wg * 4 + 4; ++q) {
-          float v[16];
-          tmem_ld16(tmem_addr(tCB + J * 128, wlane, q * 16), v);
-          uint32_t pk[8];
+        for (int q = wg * 2; q < wg * 2 + 2; ++q) {
+          uint32_t pk[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          if (J * kRows + q * 16 <= warp_last_row && J * kRows + q * 16 < len) {  // else all masked
+            float v[16];
+            tmem_ld16(tmem_addr(tCB + J * 128, wlane, q * 16), v);
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            float a2[2];
+            for (int e = 0; e < 16; e += 2) {
+              float a2[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int j = J * kRows + q * 16 + e + u;
-              a2[u] = (row_ok && j <= i && sq[j] == si) ? v[e + u] * __expf(li - lb[j]) * db[j] : 0.0f;
+              for (int u = 0; u < 2; ++u) {
+                const int j = J * kRows + q * 16 + e + u;
+                a2[u] = (row_ok && j <= i && sq[j] == si) ? v[e + u] * __expf(li - lb[j]) * db[j] : 0.0f;
+              }
+              pk[e / 2] = pack_bf16x2(a2[0], a2[1]);
             }
-            pk[e / 2] = pack_bf16x2(a2[0], a2[1]);
           }
           uint8_t* blk = aJ + (q / 4) * (kRows * 128);
           const uint32_t e0 = (q % 4) * 16;
@@ -260,13 +287,19 @@ __global__ void __launch_bounds__(kThr, 1) chunk_scan_tc_kernel(Plan p, Bufs f,
       mma_ck(d2, sC, sH + buf * hbytes, p.N, id64, true);  // Y2 = C_I H^T
       mma_commit(&bar[2 + buf]);
     }
-    if (hh > 0) epilogue(hh - 1);
+    if (hh > 0) epilogue(hh - 1, xcur, li_prev);
+    li_prev = row_ok ? lq[(hh % 3) * p.Q + i] : 0.0f;
+    if (pre < hpg && tq < p.Q) {
+      lq[(pre % 3) * p.Q + tq] = pl;
+      dq[(pre % 3) * p.Q + tq] = pd;
+    }
   }
   {
     const int last = hpg - 1;
+    fetch_x(last, xprev);
     if (!mbar_wait(&bar[2 + (last & 1)], (last >> 1) & 1)) ok = false;
     tc_fence_after();
-    epilogue(last);
+    epilogue(last, xprev, li_prev);
   }
   if (!ok) atomicOr(&f.hdr->status, kDevTimeout);
   tc_fence_before();
@@ -301,7 +334,7 @@ cudaError_t launch_chunk_scan_tc(const Plan& p, const Bufs& f, cudaStream_t s) {
       !encode_tmap_bf16_4d(&tmX, f.x, dxx, sxx, bxx, 128) ||
       !encode_tmap_bf16_4d(&tmH, f.Hin, dh, sh, bh, 128))
     return cudaErrorInvalidValue;
-  const size_t smem = 1024 + G.bytes + 5 * p.Q * 4 + 64;
+  const size_t smem = 1024 + G.bytes + 7 * p.Q * 4 + 64;
   cudaError_t e = cudaFuncSetAttribute(chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
 
 cudaError_t launch_state_passing(const Plan& p, const Bufs& f, bool backward, bool keep_f32, cudaStream_t s) {
   const unsigned tiles = (unsigned)p.sp_chains * p.sp_nseg;
-  set_kernel_name(backward ? "state_passing_bwd" : "state_passing_fwd");
+  set_kernel_name(backward ? "state_passing_bwd" : (keep_f32 ? "state_passing_fwd_keep" : "state_passing_fwd"));
   const bool bf = p.dtype == SSD_BF16;
   if (backward) {
     if (bf) state_passing_kernel<true, false, __nv_bfloat16><<<tiles, kSpThreads, 0, s>>>(p, f);
