@@ -41,8 +41,8 @@ namespace {
 using namespace tc;
 
 constexpr int kRows = 128;
-constexpr int kThr = 512;  // 16 warps: four read each quarter of the tensor-memory lanes
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kCompute = 512;        // 16 compute warps: four read each quarter of the TMEM lanes
+constexpr int kThr = kCompute + 32;  // and one control warp that issues the copies and MMAs
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kTok = kRows * 128u;  // one (128 tokens x 64) bf16 tile
 
@@ -82,49 +82,6 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
 }
 
-// Column sums of a 32-row x 16-column block held one row per lane: after the
-// call, lane l holds the sum over the warp's 32 rows of column
-// 8*b4 + 4*b3 + 2*b2 + b1 (b_k = bit k of l).  Fixed butterfly order.
-__device__ __forceinline__ float colsum16(float (&v)[16], int lane) {
-  float a8[8];
-  const bool hi16 = lane & 16;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float send = hi16 ? v[k] : v[8 + k];
-    const float keep = hi16 ? v[8 + k] : v[k];
-    a8[k] = keep + __shfl_xor_sync(kFull, send, 16);
-  }
-  float a4[4];
-  const bool hi8 = lane & 8;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float send = hi8 ? a8[k] : a8[4 + k];
-    const float keep = hi8 ? a8[4 + k] : a8[k];
-    a4[k] = keep + __shfl_xor_sync(kFull, send, 8);
-  }
-  float a2[2];
-  const bool hi4 = lane & 4;
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const float send = hi4 ? a4[k] : a4[2 + k];
-    const float keep = hi4 ? a4[2 + k] : a4[k];
-    a2[k] = keep + __shfl_xor_sync(kFull, send, 4);
-  }
-  const bool hi2 = lane & 2;
-  const float send = hi2 ? a2[0] : a2[1];
-  const float keep = hi2 ? a2[1] : a2[0];
-  float a1 = keep + __shfl_xor_sync(kFull, send, 2);
-  a1 += __shfl_xor_sync(kFull, a1, 1);
-  return a1;
-}
-
-__device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t& ph) {
-  const bool r = mbar_wait(bar, ph);
-  ph ^= 1;
-  tc_fence_after();
-  return r;
-}
-
 // Butterfly sum over the 32 lanes, in a fixed order.
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -151,10 +108,44 @@ __device__ __forceinline__ void zero_padding(const GTiles& T, uint8_t* sXb, uint
   }
 }
 
-// Shared-memory words after the tiles: l*log2(e) and dt of two heads, the
-// segment ids, the partial-sum arrays of the token kernel, then barriers.
-__host__ __device__ inline size_t group_smem_bytes(const GTiles& T, int Q) {
-  return 1024 + T.offF + (size_t)(5 * Q + 24 * kRows + 8) * 4 + 8 * 8 + 16;
+// Shared-memory bytes: the tiles, then l and dt of two heads, the segment
+// ids, the partial-sum arrays of the token kernel, the barriers and the D of
+// the group's heads.
+__host__ __device__ inline size_t group_smem_bytes(const GTiles& T, int Q, int hpg) {
+  return 1024 + T.offF + (size_t)(5 * Q + 24 * kRows + 8) * 4 + 10 * 8 + 16 + (size_t)hpg * 4 + 16;
+}
+
+// Column sums of a 32-row x 8-column block held one row per lane: after the
+// call, lane l holds the sum over the warp's 32 rows of column
+// 4*b4 + 2*b3 + b2 (b_k = bit k of l).  Fixed butterfly order.
+__device__ __forceinline__ float colsum8(float (&v)[8], int lane) {
+  float a4[4];
+  const bool hi16 = lane & 16;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float send = hi16 ? v[k] : v[4 + k];
+    const float keep = hi16 ? v[4 + k] : v[k];
+    a4[k] = keep + __shfl_xor_sync(kFull, send, 16);
+  }
+  float a2[2];
+  const bool hi8 = lane & 8;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float send = hi8 ? a4[k] : a4[2 + k];
+    const float keep = hi8 ? a4[2 + k] : a4[k];
+    a2[k] = keep + __shfl_xor_sync(kFull, send, 8);
+  }
+  const bool hi4 = lane & 4;
+  const float send = hi4 ? a2[0] : a2[1];
+  const float keep = hi4 ? a2[1] : a2[0];
+  float a1 = keep + __shfl_xor_sync(kFull, send, 4);
+  a1 += __shfl_xor_sync(kFull, a1, 2);
+  a1 += __shfl_xor_sync(kFull, a1, 1);
+  return a1;
+}
+
+__device__ __forceinline__ void named_sync_compute() {  // the 16 compute warps only
+  asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
 }
 
 __global__ void __launch_bounds__(kThr, 1) chunk_bwd_group_tc_kernel(Plan p, Bufs f,
@@ -174,8 +165,8 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_group_tc_kernel(Plan p, Buf
   uint8_t* sYb = sm + T.offY;
   uint8_t* sS = sm + T.offS;
   uint8_t* sH = sm + T.offH;
-  float* l2q = reinterpret_cast<float*>(sm + T.offF);  // [2 slots][Q] l * log2(e) of a head
-  float* dtq = l2q + 2 * p.Q;                         // [2 slots][Q] dt of a head
+  float* lq = reinterpret_cast<float*>(sm + T.offF);  // [2 slots][Q] l of a head
+  float* dtq = lq + 2 * p.Q;                          // [2 slots][Q] dt of a head
   int* sq = reinterpret_cast<int*>(dtq + 2 * p.Q);    // [Q] segment ids
   float* colR = reinterpret_cast<float*>(sq + p.Q);   // [4 lane quarters][128] column sums of R
   float* colQ = colR + 4 * kRows;                     // [4][128] column sums of dM (C.B) E
@@ -184,25 +175,58 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_group_tc_kernel(Plan p, Buf
   float* duP = carP + 4 * kRows;                      // [4][128] x . dS B, by headdim quarter
   float* dyxP = duP + 4 * kRows;                      // [4][128] dy . x, by headdim quarter
   float* red = dyxP + 4 * kRows;                      // [8] per-warp sums
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 8);  // ld_bc, ld_xy[2], ld_sh, batch1, dX
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 6);
+  // ld_bc, xy[2], sh, b1 (batch 1 done), dx (dX done), mready (M tile written), edone (epilogue read)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 8);
+  uint64_t *b_bc = bar, *b_xy = bar + 1, *b_sh = bar + 3, *b_b1 = bar + 4, *b_dx = bar + 5, *b_mr = bar + 6,
+           *b_ed = bar + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 8);
+  float* sD = reinterpret_cast<float*>(tmem_slot + 4);  // [hpg] D of the group's heads
 
   const int c = blockIdx.x, g = blockIdx.y, bi = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31;
-  const int wg = tid >> 7, r = tid & 127, wq = (tid >> 5) & 3;
+  const bool ctl = tid >= kCompute;
+  const int wg = (tid >> 7) & 3, r = tid & 127, wq = (tid >> 5) & 3;
   const int wlane = wq * 32;
   const int t0 = c * p.Q, len = min(p.Q, p.L - t0);
   const int hpg = p.hpg, h_first = g * hpg;
   const long long bh0 = (long long)bi * p.H + h_first;
-
+  const uint32_t tok_bytes = (uint32_t)T.rows * 128u;
+  const uint32_t c_bytes = (uint32_t)T.ncb * T.rows * T.cw;
+  const uint32_t s_bytes = (uint32_t)p.N * 128u;
+  auto issue_xy = [&](int hh) {
+    const int buf = hh & 1, h = h_first + hh;
+    mbar_expect_tx(&b_xy[buf], 2 * tok_bytes);
+    tma_load_4d(sXb + buf * kTok, &tmX, &b_xy[buf], 0, h, t0, bi);
+    tma_load_4d(sYb + buf * kTok, &tmY, &b_xy[buf], 0, h, t0, bi);
+  };
+  auto issue_sh = [&](int hh) {
+    const int h = h_first + hh;
+    mbar_expect_tx(b_sh, 2 * s_bytes);
+    tma_load_4d(sS, &tmS, b_sh, 0, 0, c, bi * p.H + h);
+    tma_load_4d(sH, &tmH, b_sh, 0, 0, c, bi * p.H + h);
+  };
+  if (tid == kCompute) {  // the control lane starts the tile copies first
+    for (int k = 0; k < 4; ++k) mbar_init(&bar[k], 1);
+    mbar_fence_init();
+    mbar_expect_tx(b_bc, 2 * c_bytes);
+    for (int q = 0; q < T.ncb; ++q) {
+      tma_load_4d(sB + q * T.cblk, &tmB, b_bc, q * 64, g, t0, bi);
+      tma_load_4d(sC + q * T.cblk, &tmC, b_bc, q * 64, g, t0, bi);
+    }
+    issue_xy(0);
+    if (hpg > 1) issue_xy(1);
+    issue_sh(0);
+  }
   for (int t = tid; t < p.Q; t += kThr) sq[t] = t < len ? seg_of(p, f, bi, (long long)t0 + t) : -1;
   if (tid < p.Q) {  // scalars of the group's first head into slot 0
-    l2q[tid] = f.lcs[bh0 * p.Lp + t0 + tid] * kLog2e;
+    lq[tid] = f.lcs[bh0 * p.Lp + t0 + tid];
     dtq[tid] = f.dte[bh0 * p.Lp + t0 + tid];
   }
-  zero_padding(T, sXb, sYb, sB, sC, tid);
+  for (int k = tid; k < hpg; k += kThr) sD[k] = f.D[h_first + k];
+  zero_padding(T, sXb, sYb, sB, sC, tid);  // rows the tensor copies never write
   if (tid == 0) {
-    for (int k = 0; k < 6; ++k) mbar_init(&bar[k], 1);
+    for (int k = 4; k < 7; ++k) mbar_init(&bar[k], 1);
+    mbar_init(b_ed, 1);
     mbar_fence_init();
   }
   if (tid < 32) tmem_alloc(tmem_slot, 512);
@@ -213,242 +237,243 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_group_tc_kernel(Plan p, Buf
   const uint32_t tm = *tmem_slot;
   // C B^T | dM | dX | dXs (two buffers) | Yc
   const uint32_t tCB = tm, tDM = tm + 128, tDX = tm + 256, tDXS = tm + 320, tYC = tm + 448;
-  const int s_in = seg_in_of(p, f, bi, c);
-  const int s_last = sq[len - 1];
-  const bool one_seg = sq[0] == s_last;  // seq_idx is nondecreasing: no reset inside the chunk
   bool ok = true;
-  uint32_t ph_m1 = 0, ph_m2 = 0;
-  const uint32_t tok_bytes = (uint32_t)T.rows * 128u;
-  const uint32_t c_bytes = (uint32_t)T.ncb * T.rows * T.cw;
-  const uint32_t s_bytes = (uint32_t)p.N * 128u;
-  const uint32_t id128 = idesc_bf16(128, 128, 0, 0), id64 = idesc_bf16(128, 64, 0, 1);
-  const uint32_t id64t = idesc_bf16(128, 64, 1, 1);
 
-  auto issue_xy = [&](int hh) {
-    const int buf = hh & 1, h = h_first + hh;
-    mbar_expect_tx(&bar[1 + buf], 2 * tok_bytes);
-    tma_load_4d(sXb + buf * kTok, &tmX, &bar[1 + buf], 0, h, t0, bi);
-    tma_load_4d(sYb + buf * kTok, &tmY, &bar[1 + buf], 0, h, t0, bi);
-  };
-  auto issue_sh = [&](int hh) {
-    const int h = h_first + hh;
-    mbar_expect_tx(&bar[3], 2 * s_bytes);
-    tma_load_4d(sS, &tmS, &bar[3], 0, 0, c, bi * p.H + h);
-    tma_load_4d(sH, &tmH, &bar[3], 0, 0, c, bi * p.H + h);
-  };
-  auto kdesc_c = [&](const uint8_t* t, int ks) {  // K-major B/C tile, K = d_state
-    const uint32_t kb = (ks * 32) / T.cw, kin = (ks * 32) % T.cw;
-    return smem_desc(smem_u32(t) + kb * T.cblk + kin, 16, 8 * T.cw, T.cswz);
-  };
-  auto kdesc_tok = [&](const uint8_t* t, int ks) {  // K-major 128 x 64 token tile, K = 64
-    return smem_desc(smem_u32(t) + ks * 32, 16, 1024, kSwz128);
-  };
-  auto mndesc_rows = [&](const uint8_t* t, int ks) {  // MN-major (64 wide), K along rows
-    return smem_desc(smem_u32(t) + ks * 16 * 128, 16, 1024, kSwz128);
-  };
-  // batch 1 of head hh: dM = dy x^T, dXs = B dS^T (buffer hh&1), Yc = C H^T
-  auto batch1 = [&](int hh) {
-    const int buf = hh & 1;
-    const uint8_t* sX = sXb + buf * kTok;
-    const uint8_t* sY = sYb + buf * kTok;
-    for (int ks = 0; ks < 4; ++ks) mma_bf16(tDM, kdesc_tok(sY, ks), kdesc_tok(sX, ks), id128, ks > 0);
-    for (int ks = 0; ks < p.N / 16; ++ks) {
-      mma_bf16(tDXS + buf * 64, kdesc_c(sB, ks), mndesc_rows(sS, ks), id64, ks > 0);
-      mma_bf16(tYC, kdesc_c(sC, ks), mndesc_rows(sH, ks), id64, ks > 0);
-    }
-    mma_commit(&bar[4]);
-  };
-
-  if (tid == 0) {
-    mbar_expect_tx(&bar[0], 2 * c_bytes);
-    for (int q = 0; q < T.ncb; ++q) {
-      tma_load_4d(sB + q * T.cblk, &tmB, &bar[0], q * 64, g, t0, bi);
-      tma_load_4d(sC + q * T.cblk, &tmC, &bar[0], q * 64, g, t0, bi);
-    }
-    issue_xy(0);
-    if (hpg > 1) issue_xy(1);
-    issue_sh(0);
-    if (!mbar_wait(&bar[0], 0)) ok = false;
-    tc_fence_after();
-    for (int ks = 0; ks < p.N / 16; ++ks)  // C B^T (M = i, N = j, K = d_state), once per group
-      mma_bf16(tCB, kdesc_c(sC, ks), kdesc_c(sB, ks), id128, ks > 0);
-    if (!mbar_wait(&bar[1], 0)) ok = false;
-    if (!mbar_wait(&bar[3], 0)) ok = false;
-    tc_fence_after();
-    batch1(0);  // its commit also covers C B^T
-  }
-
-  const int i = r;  // this thread's row (token) in the mask pass, and its token j in the epilogue
-  const bool tok_ok = i < len;
-  const int si = tok_ok ? sq[i] : -2;
-  for (int hh = 0; hh < hpg; ++hh) {
-    const int buf = hh & 1, h = h_first + hh;
-    const long long bh = bh0 + hh;
-    const uint8_t* sX = sXb + buf * kTok;
-    const uint8_t* sY = sYb + buf * kTok;
-    const float* l2 = l2q + buf * p.Q;
-    const float* dtv = dtq + buf * p.Q;
-    // scalars of head hh+1: loaded now, stored into the other slot (last read
-    // by head hh-1) before this iteration's first barrier after the epilogue
-    const bool pre = hh + 1 < hpg && tid < p.Q;
-    float nl = 0.0f, nd = 0.0f;
-    if (pre) {
-      nl = f.lcs[(bh + 1) * p.Lp + t0 + tid];
-      nd = f.dte[(bh + 1) * p.Lp + t0 + tid];
-    }
-    if (!mbar_wait(&bar[1 + buf], (hh >> 1) & 1)) ok = false;  // x, dy of head hh
-    if (!wait_mma(&bar[4], ph_m1)) ok = false;                 // batch 1 of head hh
-    if (tid == 0 && hh + 1 < hpg) issue_sh(hh + 1);            // dS, H have been consumed
-    const float li2 = tok_ok ? l2[i] : 0.0f;
-    // ---- mask pass: row i, columns 32 wg .. 32 wg + 31
-    {
-      float racc = 0.0f;
-      for (int q = wg * 2; q < wg * 2 + 2; ++q) {
-        uint32_t pk[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        float cr = 0.0f, cq = 0.0f;
-        if (q * 16 <= wlane + 31 && q * 16 < len) {  // warp-uniform; else every entry is masked
-          float cb[16], dm[16], rv[16], qv[16];
-          tmem_ld16x2(tmem_addr(tCB, wlane, q * 16), tmem_addr(tDM, wlane, q * 16), cb, dm);
-#pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const int j = q * 16 + e;
-            const float2 lj = *reinterpret_cast<const float2*>(l2 + j);
-            const float2 dj = *reinterpret_cast<const float2*>(dtv + j);
-            const bool v0 = tok_ok && j <= i && (one_seg || sq[j] == si);
-            const bool v1 = tok_ok && j + 1 <= i && (one_seg || sq[j + 1] == si);
-            const float2 E = make_float2(exp2f(v0 ? li2 - lj.x : -INFINITY), exp2f(v1 ? li2 - lj.y : -INFINITY));
-            const float2 cbE = __fmul2_rn(make_float2(cb[e], cb[e + 1]), E);
-            const float2 m = __fmul2_rn(cbE, dj);
-            const float2 dm2 = make_float2(dm[e], dm[e + 1]);
-            const float2 rr = __fmul2_rn(dm2, m);
-            const float2 qq = __fmul2_rn(dm2, cbE);
-            rv[e] = rr.x;
-            rv[e + 1] = rr.y;
-            qv[e] = qq.x;
-            qv[e + 1] = qq.y;
-            racc += rr.x;
-            racc += rr.y;
-            pk[e / 2] = pack2(m.x, m.y);
-          }
-          cr = colsum16(rv, lane);
-          cq = colsum16(qv, lane);
+  if (ctl) {
+    // ---------------- control warp: one lane issues every copy and MMA ----------------
+    if (lane == 0) {
+      const uint32_t id128 = idesc_bf16(128, 128, 0, 0), id64 = idesc_bf16(128, 64, 0, 1);
+      const uint32_t id64t = idesc_bf16(128, 64, 1, 1);
+      auto kdesc_c = [&](const uint8_t* t, int ks) {  // K-major B/C tile, K = d_state
+        const uint32_t kb = (ks * 32) / T.cw, kin = (ks * 32) % T.cw;
+        return smem_desc(smem_u32(t) + kb * T.cblk + kin, 16, 8 * T.cw, T.cswz);
+      };
+      auto kdesc_tok = [&](const uint8_t* t, int ks) {  // K-major 128 x 64 token tile, K = 64
+        return smem_desc(smem_u32(t) + ks * 32, 16, 1024, kSwz128);
+      };
+      auto mndesc_rows = [&](const uint8_t* t, int ks) {  // MN-major (64 wide), K along rows
+        return smem_desc(smem_u32(t) + ks * 16 * 128, 16, 1024, kSwz128);
+      };
+      // batch 1 of head hh: dM = dy x^T, dXs = B dS^T (buffer hh&1), Yc = C H^T
+      auto batch1 = [&](int hh) {
+        const int buf = hh & 1;
+        const uint8_t* sX = sXb + buf * kTok;
+        const uint8_t* sY = sYb + buf * kTok;
+        for (int ks = 0; ks < 4; ++ks) mma_bf16(tDM, kdesc_tok(sY, ks), kdesc_tok(sX, ks), id128, ks > 0);
+        for (int ks = 0; ks < p.N / 16; ++ks) {
+          mma_bf16(tDXS + buf * 64, kdesc_c(sB, ks), mndesc_rows(sS, ks), id64, ks > 0);
+          mma_bf16(tYC, kdesc_c(sC, ks), mndesc_rows(sH, ks), id64, ks > 0);
         }
-        uint8_t* blk = sA + (q / 4) * kTok;
-        const uint32_t e0 = (q % 4) * 16;
-        *reinterpret_cast<uint4*>(blk + swz128_off(i, e0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4*>(blk + swz128_off(i, e0 + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        if ((lane & 1) == 0) {
-          const int col = q * 16 + ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 +
-                          ((lane >> 1) & 1);
-          colR[wq * kRows + col] = cr;
-          colQ[wq * kRows + col] = cq;
-        }
-      }
-      rowR[wg * kRows + i] = racc;
-    }
-    {  // carry term of dl_i: cv_i e^{l_i} dy_i . Yc_i (headdim columns 16 wg .. 16 wg + 15)
-      float yc[16];
-      tmem_ld16(tmem_addr(tYC, wlane, wg * 16), yc);
-      const uint4 a = *reinterpret_cast<const uint4*>(sY + swz128_off(i, wg * 16));
-      const uint4 b = *reinterpret_cast<const uint4*>(sY + swz128_off(i, wg * 16 + 8));
-      const uint32_t dy[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      float s = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float2 d = unpack2(dy[e]);
-        s += d.x * yc[2 * e] + d.y * yc[2 * e + 1];
-      }
-      carP[wg * kRows + i] = (tok_ok && si == s_in) ? exp2f(li2) * s : 0.0f;
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();  // the M tile is complete; dM and Yc have been read
-    if (tid == 0) {
+        mma_commit(b_b1);
+      };
+      if (!mbar_wait(b_bc, 0)) ok = false;
       tc_fence_after();
-      for (int ks = 0; ks < kRows / 16; ++ks) {  // dX = M^T dy (M = j, N = 64, K = tokens i)
-        const uint64_t da = smem_desc(smem_u32(sA) + ks * 16 * 128, kTok, 1024, kSwz128);
-        mma_bf16(tDX, da, mndesc_rows(sY, ks), id64t, ks > 0);
-      }
-      mma_commit(&bar[5]);
-      if (hh + 1 < hpg) {  // batch 1 of the next head runs under this head's epilogue
-        if (!mbar_wait(&bar[1 + (buf ^ 1)], ((hh + 1) >> 1) & 1)) ok = false;
-        if (!mbar_wait(&bar[3], (hh + 1) & 1)) ok = false;
-        tc_fence_after();
-        batch1(hh + 1);
-      }
-    }
-    // dl and ddt_eff partial sums of this head (token t = r, warpgroup 0)
-    float dl_t = 0.0f, dd_t = 0.0f;
-    if (wg == 0) {
-      const int t = r;
-      dl_t = ((rowR[t] + rowR[kRows + t]) + (rowR[2 * kRows + t] + rowR[3 * kRows + t])) +
-             ((carP[t] + carP[kRows + t]) + (carP[2 * kRows + t] + carP[3 * kRows + t])) -
-             ((colR[t] + colR[kRows + t]) + (colR[2 * kRows + t] + colR[3 * kRows + t]));
-      dd_t = (colQ[t] + colQ[kRows + t]) + (colQ[2 * kRows + t] + colQ[3 * kRows + t]);
-    }
-    if (!wait_mma(&bar[5], ph_m2)) ok = false;  // dX of head hh
-    // ---- epilogue: token j = r, headdim columns 16 wg .. 16 wg + 15
-    {
-      const int j = r;
-      const float w = (tok_ok && sq[j] == s_last) ? exp2f(l2[len - 1] - l2[j]) : 0.0f;
-      const float u = w * (tok_ok ? dtv[j] : 0.0f);
-      const float Dh = f.D[h];
-      float du = 0.0f, dyx = 0.0f;
-      __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(f.dx);
-      const long long xrow = (((long long)bi * p.L + t0 + j) * p.H + h) * 64;
-      const int q = wg;
-      float a[16], s[16];
-      tmem_ld16x2(tmem_addr(tDX, wlane, q * 16), tmem_addr(tDXS + buf * 64, wlane, q * 16), a, s);
-      const uint4 x0 = *reinterpret_cast<const uint4*>(sX + swz128_off(j, q * 16));
-      const uint4 x1 = *reinterpret_cast<const uint4*>(sX + swz128_off(j, q * 16 + 8));
-      const uint4 y0 = *reinterpret_cast<const uint4*>(sY + swz128_off(j, q * 16));
-      const uint4 y1 = *reinterpret_cast<const uint4*>(sY + swz128_off(j, q * 16 + 8));
-      const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      const uint32_t ys[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-      uint32_t o[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float2 xv = unpack2(xs[e]), yv = unpack2(ys[e]);
-        du += xv.x * s[2 * e] + xv.y * s[2 * e + 1];
-        dyx += xv.x * yv.x + xv.y * yv.y;
-        o[e] = pack2(a[2 * e] + u * s[2 * e] + Dh * yv.x, a[2 * e + 1] + u * s[2 * e + 1] + Dh * yv.y);
-      }
-      if (tok_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(dx + xrow + q * 16);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-      }
-      duP[wg * kRows + j] = du;
-      dyxP[wg * kRows + j] = tok_ok ? dyx : 0.0f;
-      if (pre) {
-        l2q[(buf ^ 1) * p.Q + tid] = nl * kLog2e;
-        dtq[(buf ^ 1) * p.Q + tid] = nd;
-      }
-      __syncthreads();
-      if (wg == 0) {
-        const float du_t = (duP[j] + duP[kRows + j]) + (duP[2 * kRows + j] + duP[3 * kRows + j]);
-        float udu = 0.0f;
-        if (tok_ok) {
-          dd_t += w * du_t;
-          dl_t -= u * du_t;
-          udu = u * du_t;
-          f.ddte[bh * p.Lp + t0 + j] = dd_t;
-          f.dl[bh * p.Lp + t0 + j] = dl_t;
+      for (int ks = 0; ks < p.N / 16; ++ks)  // C B^T (M = i, N = j, K = d_state), once per group
+        mma_bf16(tCB, kdesc_c(sC, ks), kdesc_c(sB, ks), id128, ks > 0);
+      if (!mbar_wait(&b_xy[0], 0)) ok = false;
+      if (!mbar_wait(b_sh, 0)) ok = false;
+      tc_fence_after();
+      batch1(0);  // its commit also covers C B^T
+      for (int hh = 0; hh < hpg; ++hh) {
+        const int buf = hh & 1;
+        if (hh >= 1 && hh + 1 < hpg) {  // x, dy of head hh+1 into the buffer head hh-1 used, once its
+          // epilogue has read them (that epilogue waited for the head's MMAs)
+          if (!mbar_wait(b_ed, (hh - 1) & 1)) ok = false;
+          issue_xy(hh + 1);
         }
-        udu = warp_sum(udu);
-        if (lane == 0) red[wq] = udu;
-      } else if (wg == 1) {
-        float v = (dyxP[j] + dyxP[kRows + j]) + (dyxP[2 * kRows + j] + dyxP[3 * kRows + j]);
-        v = warp_sum(v);
-        if (lane == 0) red[4 + wq] = v;
+        if (hh + 1 < hpg) {  // dS, H of head hh+1 once batch 1 of head hh has read them
+          if (!mbar_wait(b_b1, hh & 1)) ok = false;
+          issue_sh(hh + 1);
+        }
+        if (!mbar_wait(b_mr, hh & 1)) ok = false;  // M tile of head hh written; dM, Yc read back
+        tc_fence_after();
+        const uint8_t* sY = sYb + buf * kTok;
+        for (int ks = 0; ks < kRows / 16; ++ks) {  // dX = M^T dy (M = j, N = 64, K = tokens i)
+          const uint64_t da = smem_desc(smem_u32(sA) + ks * 16 * 128, kTok, 1024, kSwz128);
+          mma_bf16(tDX, da, mndesc_rows(sY, ks), id64t, ks > 0);
+        }
+        mma_commit(b_dx);
+        if (hh + 1 < hpg) {  // batch 1 of the next head runs under this head's epilogue; its dXs
+          // buffer was last read by the epilogue of head hh-1
+          if (hh >= 1 && !mbar_wait(b_ed, (hh - 1) & 1)) ok = false;
+          if (!mbar_wait(&b_xy[buf ^ 1], ((hh + 1) >> 1) & 1)) ok = false;
+          if (!mbar_wait(b_sh, (hh + 1) & 1)) ok = false;
+          tc_fence_after();
+          batch1(hh + 1);
+        }
       }
     }
-    tc_fence_before();
-    __syncthreads();  // TMEM dX and the shared partials are reused by the next head
-    if (tid == 0) {
+  } else {
+    // ---------------- 16 compute warps: mask pass and epilogue ----------------
+    const int s_in = seg_in_of(p, f, bi, c);
+    const int s_last = sq[len - 1];
+    const bool one_seg = sq[0] == s_last;  // seq_idx is nondecreasing: no reset inside the chunk
+    const int i = r;  // this thread's row (token) in the mask pass, and its token j in the epilogue
+    const bool tok_ok = i < len;
+    const int si = tok_ok ? sq[i] : -2;
+    const int lim = tok_ok ? i : -1;  // columns j <= lim are on or below the diagonal
+    uint32_t ph_b1 = 0, ph_dx = 0;
+    for (int hh = 0; hh < hpg; ++hh) {
+      const int buf = hh & 1, h = h_first + hh;
+      const long long bh = bh0 + hh;
+      const uint8_t* sX = sXb + buf * kTok;
+      const uint8_t* sY = sYb + buf * kTok;
+      const float* lb = lq + buf * p.Q;
+      const float* db = dtq + buf * p.Q;
+      // scalars of head hh+1 into the other slot (last read by head hh-1, whose
+      // readers all passed the previous iteration's barriers)
+      if (hh + 1 < hpg && tid < p.Q) {
+        cp_async4(lq + (buf ^ 1) * p.Q + tid, f.lcs + (bh + 1) * p.Lp + t0 + tid);
+        cp_async4(dtq + (buf ^ 1) * p.Q + tid, f.dte + (bh + 1) * p.Lp + t0 + tid);
+      }
+      cp_async_commit();
+      if (!mbar_wait(&b_xy[buf], (hh >> 1) & 1)) ok = false;  // x, dy of head hh
+      if (!mbar_wait(b_b1, ph_b1)) ok = false;                // dM, dXs, Yc of head hh
+      ph_b1 ^= 1;
+      tc_fence_after();
+      const float li = tok_ok ? lb[i] : 0.0f;
+      // ---- mask pass: row i, columns 32 wg .. 32 wg + 31 in 8-column steps
+      {
+        float racc = 0.0f;
+        for (int q8 = wg * 4; q8 < wg * 4 + 4; ++q8) {
+          const int j0 = q8 * 8;
+          uint32_t pk[4] = {0, 0, 0, 0};
+          float cr = 0.0f, cq = 0.0f;
+          if (j0 <= wlane + 31 && j0 < len) {  // warp-uniform; else every entry is masked
+            float cb[8], dm[8], rv[8], qv[8];
+            tmem_ld8x2(tmem_addr(tCB, wlane, j0), tmem_addr(tDM, wlane, j0), cb, dm);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const float4 lj = *reinterpret_cast<const float4*>(lb + j0 + 4 * k);
+              const float4 dj = *reinterpret_cast<const float4*>(db + j0 + 4 * k);
+              int4 sj = make_int4(si, si, si, si);
+              if (!one_seg) sj = *reinterpret_cast<const int4*>(sq + j0 + 4 * k);
+              const float lv[4] = {lj.x, lj.y, lj.z, lj.w}, dv[4] = {dj.x, dj.y, dj.z, dj.w};
+              const int sv[4] = {sj.x, sj.y, sj.z, sj.w};
+              float mv[4];
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const int e = 4 * k + m;
+                const bool on = j0 + e <= lim && sv[m] == si;
+                const float cbE = cb[e] * __expf(on ? li - lv[m] : -INFINITY);
+                mv[m] = cbE * dv[m];
+                rv[e] = dm[e] * mv[m];
+                qv[e] = dm[e] * cbE;
+                racc += rv[e];
+              }
+              pk[2 * k] = pack2(mv[0], mv[1]);
+              pk[2 * k + 1] = pack2(mv[2], mv[3]);
+            }
+            cr = colsum8(rv, lane);
+            cq = colsum8(qv, lane);
+          }
+          uint8_t* blk = sA + (q8 / 8) * kTok;
+          *reinterpret_cast<uint4*>(blk + swz128_off(i, (q8 % 8) * 8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          if ((lane & 3) == 0) {
+            const int col = j0 + ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+            colR[wq * kRows + col] = cr;
+            colQ[wq * kRows + col] = cq;
+          }
+        }
+        rowR[wg * kRows + i] = racc;
+      }
+      {  // carry term of dl_i: cv_i e^{l_i} dy_i . Yc_i (headdim columns 16 wg .. 16 wg + 15)
+        float yc[16];
+        tmem_ld16(tmem_addr(tYC, wlane, wg * 16), yc);
+        const uint4 a = *reinterpret_cast<const uint4*>(sY + swz128_off(i, wg * 16));
+        const uint4 b = *reinterpret_cast<const uint4*>(sY + swz128_off(i, wg * 16 + 8));
+        const uint32_t dy[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float s = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 d = unpack2(dy[e]);
+          s += d.x * yc[2 * e] + d.y * yc[2 * e + 1];
+        }
+        carP[wg * kRows + i] = (tok_ok && si == s_in) ? __expf(li) * s : 0.0f;
+      }
+      const float w = (tok_ok && sq[i] == s_last) ? __expf(lb[len - 1] - li) : 0.0f;
+      const float u = w * (tok_ok ? db[i] : 0.0f);
+      cp_async_wait_all();  // this thread's scalar copies of head hh+1 have landed
+      fence_async_smem();
+      tc_fence_before();
+      named_sync_compute();  // M tile and partials complete; dM and Yc read back
+      if (tid == 0) {
+        mbar_arrive(b_mr);
+        if (hh > 0) {  // per-chunk sums of head hh-1 (written before this barrier)
+          f.udu[(bh - 1) * p.nc + c] = (red[0] + red[1]) + (red[2] + red[3]);
+          f.pdD[((long long)bi * p.nc + c) * p.H + h - 1] = (red[4] + red[5]) + (red[6] + red[7]);
+        }
+      }
+      // dl and ddt_eff partial sums of this head (token t = r, warpgroup 0)
+      float dl_t = 0.0f, dd_t = 0.0f;
+      if (wg == 0) {
+        const int t = r;
+        dl_t = ((rowR[t] + rowR[kRows + t]) + (rowR[2 * kRows + t] + rowR[3 * kRows + t])) +
+               ((carP[t] + carP[kRows + t]) + (carP[2 * kRows + t] + carP[3 * kRows + t])) -
+               ((colR[t] + colR[kRows + t]) + (colR[2 * kRows + t] + colR[3 * kRows + t]));
+        dd_t = (colQ[t] + colQ[kRows + t]) + (colQ[2 * kRows + t] + colQ[3 * kRows + t]);
+      }
+      if (!mbar_wait(b_dx, ph_dx)) ok = false;  // dX of head hh
+      ph_dx ^= 1;
+      tc_fence_after();
+      // ---- epilogue: token j = r, headdim columns 16 wg .. 16 wg + 15
+      {
+        const int j = r;
+        const float Dh = sD[hh];
+        float du = 0.0f, dyx = 0.0f;
+        __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(f.dx);
+        const long long xrow = (((long long)bi * p.L + t0 + j) * p.H + h) * 64;
+        const int q = wg;
+        float a[16], s[16];
+        tmem_ld16x2(tmem_addr(tDX, wlane, q * 16), tmem_addr(tDXS + buf * 64, wlane, q * 16), a, s);
+        const uint4 x0 = *reinterpret_cast<const uint4*>(sX + swz128_off(j, q * 16));
+        const uint4 x1 = *reinterpret_cast<const uint4*>(sX + swz128_off(j, q * 16 + 8));
+        const uint4 y0 = *reinterpret_cast<const uint4*>(sY + swz128_off(j, q * 16));
+        const uint4 y1 = *reinterpret_cast<const uint4*>(sY + swz128_off(j, q * 16 + 8));
+        const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint32_t ys[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 xv = unpack2(xs[e]), yv = unpack2(ys[e]);
+          du += xv.x * s[2 * e] + xv.y * s[2 * e + 1];
+          dyx += xv.x * yv.x + xv.y * yv.y;
+          o[e] = pack2(a[2 * e] + u * s[2 * e] + Dh * yv.x, a[2 * e + 1] + u * s[2 * e + 1] + Dh * yv.y);
+        }
+        if (tok_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(dx + xrow + q * 16);
+          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        duP[wg * kRows + j] = du;
+        dyxP[wg * kRows + j] = tok_ok ? dyx : 0.0f;
+        tc_fence_before();
+        named_sync_compute();  // dX, dXs, x, dy of this head read back; du, dy.x partials complete
+        if (tid == 0) mbar_arrive(b_ed);
+        if (wg == 0) {
+          const float du_t = (duP[j] + duP[kRows + j]) + (duP[2 * kRows + j] + duP[3 * kRows + j]);
+          float udu = 0.0f;
+          if (tok_ok) {
+            dd_t += w * du_t;
+            dl_t -= u * du_t;
+            udu = u * du_t;
+            f.ddte[bh * p.Lp + t0 + j] = dd_t;
+            f.dl[bh * p.Lp + t0 + j] = dl_t;
+          }
+          udu = warp_sum(udu);
+          if (lane == 0) red[wq] = udu;
+        } else if (wg == 1) {
+          float v = (dyxP[j] + dyxP[kRows + j]) + (dyxP[2 * kRows + j] + dyxP[3 * kRows + j]);
+          v = warp_sum(v);
+          if (lane == 0) red[4 + wq] = v;
+        }
+      }
+    }
+    named_sync_compute();
+    if (tid == 0) {  // per-chunk sums of the last head
+      const long long bh = bh0 + hpg - 1;
       f.udu[bh * p.nc + c] = (red[0] + red[1]) + (red[2] + red[3]);
-      f.pdD[((long long)bi * p.nc + c) * p.H + h] = (red[4] + red[5]) + (red[6] + red[7]);
-      if (hh + 2 < hpg) issue_xy(hh + 2);  // this head's x, dy buffer is free
+      f.pdD[((long long)bi * p.nc + c) * p.H + h_first + hpg - 1] = (red[4] + red[5]) + (red[6] + red[7]);
     }
   }
   if (!ok) atomicOr(&f.hdr->status, kDevTimeout);
@@ -458,14 +483,14 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_group_tc_kernel(Plan p, Buf
 }
 
 
-// dB, dC of one chunk for one group (chunk <= 128): one CTA (512 threads) per
-// (chunk, group, batch row) accumulates, in tensor memory and in fixed head
-// order,
+// dB, dC of one chunk for one group (chunk <= 128): one CTA per (chunk,
+// group, batch row) accumulates, in tensor memory and in fixed head order,
 //   dC = sum_h [ dCB_h B + diag(cv e^{l_h}) dy_h H_h ],
 //   dB = sum_h [ dCB_h^T C + diag(u_h) x_h dS_h ],   dCB_h = dM_h o E_h o dt_h.
-// Per head: dM = dy x^T is issued one head ahead; once it has run, the x and
-// dy tiles are scaled by their row factors in place and the carry and state
-// MMAs are issued; meanwhile the 16 warps form dCB (thread = row i) as a bf16
+// Warp-specialised like the token kernel: the control warp issues dM = dy x^T
+// one head ahead; once it has run, the 16 compute warps scale the x and dy
+// tiles by their row factors in place and the control warp issues the carry
+// and state MMAs, while the compute warps form dCB (thread = row i) as a bf16
 // tile that is the K-major A of dCB B and the MN-major A of dCB^T C.
 __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p, Bufs f,
                                                                         const __grid_constant__ CUtensorMap tmX,
@@ -484,28 +509,59 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
   uint8_t* sYb = sm + T.offY;
   uint8_t* sS = sm + T.offS;
   uint8_t* sH = sm + T.offH;
-  float* l2q = reinterpret_cast<float*>(sm + T.offF);  // [2 slots][Q]
-  float* dtq = l2q + 2 * p.Q;                         // [2 slots][Q]
+  float* lq = reinterpret_cast<float*>(sm + T.offF);  // [2 slots][Q]
+  float* dtq = lq + 2 * p.Q;                          // [2 slots][Q]
   int* sq = reinterpret_cast<int*>(dtq + 2 * p.Q);    // [Q]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sq + p.Q + 24 * kRows + 8);  // ld_bc, ld_xy[2], ld_sh, dm, cs, dbc
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 7);
+  // ld_bc, xy[2], sh, dm (dM done), cs (carry/state MMAs done), dbc (dB/dC MMAs done),
+  // scaled (x, dy scaled in place), dcb (dCB tile written; dM read back)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sq + p.Q + 24 * kRows + 8);
+  uint64_t *b_bc = bar, *b_xy = bar + 1, *b_sh = bar + 3, *b_dm = bar + 4, *b_cs = bar + 5, *b_dbc = bar + 6,
+           *b_sc = bar + 7, *b_dcb = bar + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
 
   const int c = blockIdx.x, g = blockIdx.y, bi = blockIdx.z;
-  const int tid = threadIdx.x;
-  const int wg = tid >> 7, r = tid & 127, wq = (tid >> 5) & 3;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const bool ctl = tid >= kCompute;
+  const int wg = (tid >> 7) & 3, r = tid & 127, wq = (tid >> 5) & 3;
   const int wlane = wq * 32;
   const int t0 = c * p.Q, len = min(p.Q, p.L - t0);
   const int hpg = p.hpg, h_first = g * hpg;
   const long long bh0 = (long long)bi * p.H + h_first;
-
+  const uint32_t tok_bytes = (uint32_t)T.rows * 128u;
+  const uint32_t c_bytes = (uint32_t)T.ncb * T.rows * T.cw;
+  const uint32_t s_bytes = (uint32_t)p.N * 128u;
+  auto issue_xy = [&](int hh) {
+    const int buf = hh & 1, h = h_first + hh;
+    mbar_expect_tx(&b_xy[buf], 2 * tok_bytes);
+    tma_load_4d(sXb + buf * kTok, &tmX, &b_xy[buf], 0, h, t0, bi);
+    tma_load_4d(sYb + buf * kTok, &tmY, &b_xy[buf], 0, h, t0, bi);
+  };
+  auto issue_sh = [&](int hh) {
+    const int h = h_first + hh;
+    mbar_expect_tx(b_sh, 2 * s_bytes);
+    tma_load_4d(sS, &tmS, b_sh, 0, 0, c, bi * p.H + h);
+    tma_load_4d(sH, &tmH, b_sh, 0, 0, c, bi * p.H + h);
+  };
+  if (tid == kCompute) {  // the control lane starts the tile copies first
+    for (int k = 0; k < 4; ++k) mbar_init(&bar[k], 1);
+    mbar_fence_init();
+    mbar_expect_tx(b_bc, 2 * c_bytes);
+    for (int q = 0; q < T.ncb; ++q) {
+      tma_load_4d(sB + q * T.cblk, &tmB, b_bc, q * 64, g, t0, bi);
+      tma_load_4d(sC + q * T.cblk, &tmC, b_bc, q * 64, g, t0, bi);
+    }
+    issue_xy(0);
+    if (hpg > 1) issue_xy(1);
+    issue_sh(0);
+  }
   for (int t = tid; t < p.Q; t += kThr) sq[t] = t < len ? seg_of(p, f, bi, (long long)t0 + t) : -1;
   if (tid < p.Q) {
-    l2q[tid] = f.lcs[bh0 * p.Lp + t0 + tid] * kLog2e;
+    lq[tid] = f.lcs[bh0 * p.Lp + t0 + tid];
     dtq[tid] = f.dte[bh0 * p.Lp + t0 + tid];
   }
   zero_padding(T, sXb, sYb, sB, sC, tid);  // B and C are contracted over tokens here
   if (tid == 0) {
-    for (int k = 0; k < 7; ++k) mbar_init(&bar[k], 1);
+    for (int k = 4; k < 9; ++k) mbar_init(&bar[k], 1);
     mbar_fence_init();
   }
   if (tid < 32) tmem_alloc(tmem_slot, 512);
@@ -515,190 +571,186 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
   tc_fence_after();
   const uint32_t tm = *tmem_slot;
   const uint32_t tDC = tm, tDB = tm + 128, tDM = tm + 256;
-  const int s_in = seg_in_of(p, f, bi, c);
-  const int s_last = sq[len - 1];
-  const bool one_seg = sq[0] == s_last;
   bool ok = true;
-  uint32_t ph_dm = 0, ph_dbc = 0;
-  const uint32_t tok_bytes = (uint32_t)T.rows * 128u;
-  const uint32_t c_bytes = (uint32_t)T.ncb * T.rows * T.cw;
-  const uint32_t s_bytes = (uint32_t)p.N * 128u;
-  const uint32_t idNk = idesc_bf16(128, p.N, 0, 0), idNmn = idesc_bf16(128, p.N, 0, 1);
-  const uint32_t idNa_mn = idesc_bf16(128, p.N, 1, 1), id128 = idesc_bf16(128, 128, 0, 0);
 
-  auto issue_xy = [&](int hh) {
-    const int buf = hh & 1, h = h_first + hh;
-    mbar_expect_tx(&bar[1 + buf], 2 * tok_bytes);
-    tma_load_4d(sXb + buf * kTok, &tmX, &bar[1 + buf], 0, h, t0, bi);
-    tma_load_4d(sYb + buf * kTok, &tmY, &bar[1 + buf], 0, h, t0, bi);
-  };
-  auto issue_sh = [&](int hh) {
-    const int h = h_first + hh;
-    mbar_expect_tx(&bar[3], 2 * s_bytes);
-    tma_load_4d(sS, &tmS, &bar[3], 0, 0, c, bi * p.H + h);
-    tma_load_4d(sH, &tmH, &bar[3], 0, 0, c, bi * p.H + h);
-  };
-  auto kdesc_tok = [&](const uint8_t* t, int ks) { return smem_desc(smem_u32(t) + ks * 32, 16, 1024, kSwz128); };
-  auto mndesc_c = [&](const uint8_t* t, int ks) {  // B/C tile as MN-major (N = d_state), K = tokens
-    return smem_desc(smem_u32(t) + ks * 16 * T.cw, T.cblk, 8 * T.cw, T.cswz);
-  };
-  auto issue_dm = [&](int hh) {  // dM = dy x^T of head hh (M = i, N = j, K = headdim)
-    const int buf = hh & 1;
-    for (int ks = 0; ks < 4; ++ks)
-      mma_bf16(tDM, kdesc_tok(sYb + buf * kTok, ks), kdesc_tok(sXb + buf * kTok, ks), id128, ks > 0);
-    mma_commit(&bar[4]);
-  };
-
-  if (tid == 0) {
-    mbar_expect_tx(&bar[0], 2 * c_bytes);
-    for (int q = 0; q < T.ncb; ++q) {
-      tma_load_4d(sB + q * T.cblk, &tmB, &bar[0], q * 64, g, t0, bi);
-      tma_load_4d(sC + q * T.cblk, &tmC, &bar[0], q * 64, g, t0, bi);
+  if (ctl) {
+    // ---------------- control warp ----------------
+    if (lane == 0) {
+      const uint32_t idNk = idesc_bf16(128, p.N, 0, 0), idNmn = idesc_bf16(128, p.N, 0, 1);
+      const uint32_t idNa_mn = idesc_bf16(128, p.N, 1, 1), id128 = idesc_bf16(128, 128, 0, 0);
+      auto kdesc_tok = [&](const uint8_t* t, int ks) { return smem_desc(smem_u32(t) + ks * 32, 16, 1024, kSwz128); };
+      auto mndesc_c = [&](const uint8_t* t, int ks) {  // B/C tile as MN-major (N = d_state), K = tokens
+        return smem_desc(smem_u32(t) + ks * 16 * T.cw, T.cblk, 8 * T.cw, T.cswz);
+      };
+      auto issue_dm = [&](int hh) {  // dM = dy x^T of head hh (M = i, N = j, K = headdim)
+        const int buf = hh & 1;
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tDM, kdesc_tok(sYb + buf * kTok, ks), kdesc_tok(sXb + buf * kTok, ks), id128, ks > 0);
+        mma_commit(b_dm);
+      };
+      if (!mbar_wait(&b_xy[0], 0)) ok = false;
+      tc_fence_after();
+      issue_dm(0);
+      for (int hh = 0; hh < hpg; ++hh) {
+        const int buf = hh & 1;
+        const uint8_t* sX = sXb + buf * kTok;
+        const uint8_t* sY = sYb + buf * kTok;
+        // carry and state: dC += (scaled dy) H, dB += (scaled x) dS  (K = headdim)
+        if (!mbar_wait(b_sc, hh & 1)) ok = false;  // x, dy of head hh scaled in place
+        if (!mbar_wait(b_sh, hh & 1)) ok = false;  // dS, H of head hh
+        tc_fence_after();
+        for (int ks = 0; ks < 4; ++ks) {
+          mma_bf16(tDC, kdesc_tok(sY, ks), kdesc_tok(sH, ks), idNk, (hh > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16(tDB, kdesc_tok(sX, ks), kdesc_tok(sS, ks), idNk, (hh > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(b_cs);
+        if (!mbar_wait(b_dcb, hh & 1)) ok = false;  // dCB of head hh written; dM read back
+        tc_fence_after();
+        if (hh + 1 < hpg) {  // dM of the next head first: the dB/dC work hides it
+          if (!mbar_wait(&b_xy[buf ^ 1], ((hh + 1) >> 1) & 1)) ok = false;
+          tc_fence_after();
+          issue_dm(hh + 1);
+        }
+        if (hh == 0 && !mbar_wait(b_bc, 0)) ok = false;  // B, C
+        tc_fence_after();
+        // dC += dCB B (A K-major, K = j);  dB += dCB^T C (A MN-major, K = i)
+        for (int ks = 0; ks < kRows / 16; ++ks) {
+          const uint64_t ak = smem_desc(smem_u32(sA) + (ks / 4) * kTok + (ks % 4) * 32, 16, 1024, kSwz128);
+          const uint64_t am = smem_desc(smem_u32(sA) + ks * 16 * 128, kTok, 1024, kSwz128);
+          mma_bf16(tDC, ak, mndesc_c(sB, ks), idNmn, 1u);
+          mma_bf16(tDB, am, mndesc_c(sC, ks), idNa_mn, 1u);
+        }
+        mma_commit(b_dbc);
+        // the carry and state MMAs of this head are done long since: release
+        // dS, H and this head's x, dy buffer to the next loads
+        if (!mbar_wait(b_cs, hh & 1)) ok = false;
+        if (hh + 1 < hpg) issue_sh(hh + 1);
+        if (hh + 2 < hpg) issue_xy(hh + 2);
+      }
     }
-    issue_xy(0);
-    if (hpg > 1) issue_xy(1);
-    issue_sh(0);
-    if (!mbar_wait(&bar[1], 0)) ok = false;
+  } else {
+    // ---------------- 16 compute warps ----------------
+    const int s_in = seg_in_of(p, f, bi, c);
+    const int s_last = sq[len - 1];
+    const bool one_seg = sq[0] == s_last;
+    const int i = r;
+    const bool tok_ok = i < len;
+    const int si = tok_ok ? sq[i] : -2;
+    const int lim = tok_ok ? i : -1;
+    uint32_t ph_dm = 0, ph_dbc = 0;
+    for (int hh = 0; hh < hpg; ++hh) {
+      const int buf = hh & 1;
+      uint8_t* sX = sXb + buf * kTok;
+      uint8_t* sY = sYb + buf * kTok;
+      const float* lb = lq + buf * p.Q;
+      const float* db = dtq + buf * p.Q;
+      if (hh + 1 < hpg && tid < p.Q) {  // scalars of head hh+1 into the other slot
+        const long long bhn = bh0 + hh + 1;
+        cp_async4(lq + (buf ^ 1) * p.Q + tid, f.lcs + bhn * p.Lp + t0 + tid);
+        cp_async4(dtq + (buf ^ 1) * p.Q + tid, f.dte + bhn * p.Lp + t0 + tid);
+      }
+      cp_async_commit();
+      if (!mbar_wait(&b_xy[buf], (hh >> 1) & 1)) ok = false;  // x, dy of head hh
+      if (!mbar_wait(b_dm, ph_dm)) ok = false;                // dM of head hh has read them
+      ph_dm ^= 1;
+      tc_fence_after();
+      // row scaling in place: warpgroups 0, 1 -> cv e^{l} dy (rows i), 2, 3 -> u x (rows j)
+      {
+        const int t = r;
+        const bool v = t < len;
+        float sc;
+        uint8_t* tile;
+        if (wg < 2) {
+          sc = (v && sq[t] == s_in) ? __expf(lb[t]) : 0.0f;
+          tile = sY;
+        } else {
+          sc = (v && sq[t] == s_last) ? __expf(lb[len - 1] - lb[t]) * db[t] : 0.0f;
+          tile = sX;
+        }
+        const float2 sc2 = make_float2(sc, sc);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t off = swz128_off(t, (wg & 1) * 32 + k * 8);
+          const uint4 w4 = *reinterpret_cast<const uint4*>(tile + off);
+          const uint32_t a[4] = {w4.x, w4.y, w4.z, w4.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 x2 = __fmul2_rn(unpack2(a[e]), sc2);
+            o[e] = pack2(x2.x, x2.y);
+          }
+          *reinterpret_cast<uint4*>(tile + off) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      fence_async_smem();
+      named_sync_compute();
+      if (tid == 0) mbar_arrive(b_sc);
+      // dCB = dM o E o dt (row i, columns 32 wg .. 32 wg + 31); the dB/dC MMAs
+      // of head hh-1 must have read the previous dCB tile first
+      if (hh > 0) {
+        if (!mbar_wait(b_dbc, ph_dbc)) ok = false;
+        ph_dbc ^= 1;
+        tc_fence_after();
+      }
+      {
+        const float li = tok_ok ? lb[i] : 0.0f;
+        for (int q = wg * 2; q < wg * 2 + 2; ++q) {
+          const int j0 = q * 16;
+          uint32_t pk[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          if (j0 <= wlane + 31 && j0 < len) {  // warp-uniform; else every entry is masked
+            float dm[16];
+            tmem_ld16(tmem_addr(tDM, wlane, j0), dm);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float4 lj = *reinterpret_cast<const float4*>(lb + j0 + 4 * k);
+              const float4 dj = *reinterpret_cast<const float4*>(db + j0 + 4 * k);
+              int4 sj = make_int4(si, si, si, si);
+              if (!one_seg) sj = *reinterpret_cast<const int4*>(sq + j0 + 4 * k);
+              const float lv[4] = {lj.x, lj.y, lj.z, lj.w}, dv[4] = {dj.x, dj.y, dj.z, dj.w};
+              const int sv[4] = {sj.x, sj.y, sj.z, sj.w};
+              float a4[4];
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const bool on = j0 + 4 * k + m <= lim && sv[m] == si;
+                a4[m] = dm[4 * k + m] * __expf(on ? li - lv[m] : -INFINITY) * dv[m];
+              }
+              pk[2 * k] = pack2(a4[0], a4[1]);
+              pk[2 * k + 1] = pack2(a4[2], a4[3]);
+            }
+          }
+          uint8_t* blk = sA + (q / 4) * kTok;
+          const uint32_t e0 = (q % 4) * 16;
+          *reinterpret_cast<uint4*>(blk + swz128_off(i, e0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(blk + swz128_off(i, e0 + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      cp_async_wait_all();  // this thread's scalar copies of head hh+1 have landed
+      fence_async_smem();
+      tc_fence_before();
+      named_sync_compute();  // dCB complete; dM read back; the other slot's scalars visible
+      if (tid == 0) mbar_arrive(b_dcb);
+    }
+    if (!mbar_wait(b_dbc, ph_dbc)) ok = false;  // the last head's dB/dC MMAs
     tc_fence_after();
-    issue_dm(0);
-  }
-
-  const int i = r;
-  const bool tok_ok = i < len;
-  const int si = tok_ok ? sq[i] : -2;
-  for (int hh = 0; hh < hpg; ++hh) {
-    const int buf = hh & 1;
-    uint8_t* sX = sXb + buf * kTok;
-    uint8_t* sY = sYb + buf * kTok;
-    const float* l2 = l2q + buf * p.Q;
-    const float* dtv = dtq + buf * p.Q;
-    const bool pre = hh + 1 < hpg && tid < p.Q;
-    float nl = 0.0f, nd = 0.0f;
-    if (pre) {
-      const long long bhn = bh0 + hh + 1;
-      nl = f.lcs[bhn * p.Lp + t0 + tid];
-      nd = f.dte[bhn * p.Lp + t0 + tid];
-    }
-    if (!mbar_wait(&bar[1 + buf], (hh >> 1) & 1)) ok = false;  // x, dy of head hh
-    if (!wait_mma(&bar[4], ph_dm)) ok = false;                 // dM of head hh has read them
-    // row scaling in place: warpgroups 0, 1 -> cv e^{l} dy (rows i), 2, 3 -> u x (rows j)
+    // epilogue: rows of dB and dC (thread = token t; d_state columns 16 q, q = wg mod 4)
     {
       const int t = r;
       const bool v = t < len;
-      float sc;
-      uint8_t* tile;
-      if (wg < 2) {
-        sc = (v && sq[t] == s_in) ? exp2f(l2[t]) : 0.0f;
-        tile = sY;
-      } else {
-        sc = (v && sq[t] == s_last) ? exp2f(l2[len - 1] - l2[t]) * dtv[t] : 0.0f;
-        tile = sX;
-      }
-      const float2 sc2 = make_float2(sc, sc);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t off = swz128_off(t, (wg & 1) * 32 + k * 8);
-        const uint4 w4 = *reinterpret_cast<const uint4*>(tile + off);
-        const uint32_t a[4] = {w4.x, w4.y, w4.z, w4.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 x2 = __fmul2_rn(unpack2(a[e]), sc2);
-          o[e] = pack2(x2.x, x2.y);
+      __nv_bfloat16* dB = static_cast<__nv_bfloat16*>(f.dB);
+      __nv_bfloat16* dC = static_cast<__nv_bfloat16*>(f.dC);
+      const long long row = (((long long)bi * p.L + t0 + t) * p.G + g) * p.N;
+      const int nq = p.N / 16;
+      for (int q = wg; q < nq; q += 4) {
+        float vb[16], vc[16];
+        tmem_ld16x2(tmem_addr(tDB, wlane, q * 16), tmem_addr(tDC, wlane, q * 16), vb, vc);
+        if (v) {
+          uint4* ob = reinterpret_cast<uint4*>(dB + row + q * 16);
+          uint4* oc = reinterpret_cast<uint4*>(dC + row + q * 16);
+          ob[0] = make_uint4(pack2(vb[0], vb[1]), pack2(vb[2], vb[3]), pack2(vb[4], vb[5]), pack2(vb[6], vb[7]));
+          ob[1] = make_uint4(pack2(vb[8], vb[9]), pack2(vb[10], vb[11]), pack2(vb[12], vb[13]), pack2(vb[14], vb[15]));
+          oc[0] = make_uint4(pack2(vc[0], vc[1]), pack2(vc[2], vc[3]), pack2(vc[4], vc[5]), pack2(vc[6], vc[7]));
+          oc[1] = make_uint4(pack2(vc[8], vc[9]), pack2(vc[10], vc[11]), pack2(vc[12], vc[13]), pack2(vc[14], vc[15]));
         }
-        *reinterpret_cast<uint4*>(tile + off) = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {  // carry and state: dC += (scaled dy) H, dB += (scaled x) dS  (K = headdim)
-      if (!mbar_wait(&bar[3], hh & 1)) ok = false;  // dS, H of head hh
-      tc_fence_after();
-      for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(tDC, kdesc_tok(sY, ks), kdesc_tok(sH, ks), idNk, (hh > 0 || ks > 0) ? 1u : 0u);
-        mma_bf16(tDB, kdesc_tok(sX, ks), kdesc_tok(sS, ks), idNk, (hh > 0 || ks > 0) ? 1u : 0u);
-      }
-      mma_commit(&bar[5]);
-    }
-    // dCB = dM o E o dt (row i, columns 32 wg .. 32 wg + 31); the dB/dC MMAs
-    // of head hh-1 must have read the previous dCB tile first
-    if (hh > 0 && !wait_mma(&bar[6], ph_dbc)) ok = false;
-    {
-      const float li2 = tok_ok ? l2[i] : 0.0f;
-      for (int q = wg * 2; q < wg * 2 + 2; ++q) {
-        uint32_t pk[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (q * 16 <= wlane + 31 && q * 16 < len) {  // warp-uniform; else every entry is masked
-          float dm[16];
-          tmem_ld16(tmem_addr(tDM, wlane, q * 16), dm);
-#pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const int j = q * 16 + e;
-            const float2 lj = *reinterpret_cast<const float2*>(l2 + j);
-            const float2 dj = *reinterpret_cast<const float2*>(dtv + j);
-            const bool v0 = tok_ok && j <= i && (one_seg || sq[j] == si);
-            const bool v1 = tok_ok && j + 1 <= i && (one_seg || sq[j + 1] == si);
-            const float2 E = make_float2(exp2f(v0 ? li2 - lj.x : -INFINITY), exp2f(v1 ? li2 - lj.y : -INFINITY));
-            const float2 v2 = __fmul2_rn(__fmul2_rn(make_float2(dm[e], dm[e + 1]), E), dj);
-            pk[e / 2] = pack2(v2.x, v2.y);
-          }
-        }
-        uint8_t* blk = sA + (q / 4) * kTok;
-        const uint32_t e0 = (q % 4) * 16;
-        *reinterpret_cast<uint4*>(blk + swz128_off(i, e0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4*>(blk + swz128_off(i, e0 + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      }
-    }
-    if (pre) {  // the other slot was last read by head hh-1
-      l2q[(buf ^ 1) * p.Q + tid] = nl * kLog2e;
-      dtq[(buf ^ 1) * p.Q + tid] = nd;
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      if (hh + 1 < hpg) {  // dM of the next head first: the tensor core has the dB/dC work to hide it
-        if (!mbar_wait(&bar[1 + (buf ^ 1)], ((hh + 1) >> 1) & 1)) ok = false;
-        tc_fence_after();
-        issue_dm(hh + 1);
-      }
-      if (hh == 0 && !mbar_wait(&bar[0], 0)) ok = false;  // B, C
-      tc_fence_after();
-      // dC += dCB B (A K-major, K = j);  dB += dCB^T C (A MN-major, K = i)
-      for (int ks = 0; ks < kRows / 16; ++ks) {
-        const uint64_t ak = smem_desc(smem_u32(sA) + (ks / 4) * kTok + (ks % 4) * 32, 16, 1024, kSwz128);
-        const uint64_t am = smem_desc(smem_u32(sA) + ks * 16 * 128, kTok, 1024, kSwz128);
-        mma_bf16(tDC, ak, mndesc_c(sB, ks), idNmn, 1u);
-        mma_bf16(tDB, am, mndesc_c(sC, ks), idNa_mn, 1u);
-      }
-      mma_commit(&bar[6]);
-      // the carry and state MMAs of this head are done long since: release
-      // dS, H and this head's x, dy buffer to the next loads
-      if (!mbar_wait(&bar[5], hh & 1)) ok = false;
-      if (hh + 1 < hpg) issue_sh(hh + 1);
-      if (hh + 2 < hpg) issue_xy(hh + 2);
-    }
-  }
-  if (!wait_mma(&bar[6], ph_dbc)) ok = false;  // the last head's dB/dC MMAs
-  // epilogue: rows of dB and dC (thread = token t; d_state columns 16 q, q = wg mod 4)
-  {
-    const int t = r;
-    const bool v = t < len;
-    __nv_bfloat16* dB = static_cast<__nv_bfloat16*>(f.dB);
-    __nv_bfloat16* dC = static_cast<__nv_bfloat16*>(f.dC);
-    const long long row = (((long long)bi * p.L + t0 + t) * p.G + g) * p.N;
-    const int nq = p.N / 16;
-    for (int q = wg; q < nq; q += 4) {
-      float vb[16], vc[16];
-      tmem_ld16x2(tmem_addr(tDB, wlane, q * 16), tmem_addr(tDC, wlane, q * 16), vb, vc);
-      if (v) {
-        uint4* ob = reinterpret_cast<uint4*>(dB + row + q * 16);
-        uint4* oc = reinterpret_cast<uint4*>(dC + row + q * 16);
-        ob[0] = make_uint4(pack2(vb[0], vb[1]), pack2(vb[2], vb[3]), pack2(vb[4], vb[5]), pack2(vb[6], vb[7]));
-        ob[1] = make_uint4(pack2(vb[8], vb[9]), pack2(vb[10], vb[11]), pack2(vb[12], vb[13]), pack2(vb[14], vb[15]));
-        oc[0] = make_uint4(pack2(vc[0], vc[1]), pack2(vc[2], vc[3]), pack2(vc[4], vc[5]), pack2(vc[6], vc[7]));
-        oc[1] = make_uint4(pack2(vc[8], vc[9]), pack2(vc[10], vc[11]), pack2(vc[12], vc[13]), pack2(vc[14], vc[15]));
       }
     }
   }
@@ -712,7 +764,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
 
 bool chunk_bwd_group_tc_supported(const Plan& p) {
   return p.dtype == SSD_BF16 && p.P == 64 && (p.Q == 64 || p.Q == 128) &&
-         (p.N == 16 || p.N == 32 || p.N == 64 || p.N == 128);
+         (p.N == 16 || p.N == 32 || p.N == 64 || p.N == 128) && p.hpg <= 256;
 }
 
 namespace {
@@ -740,7 +792,7 @@ cudaError_t launch_chunk_bwd_dbc_group_tc(const Plan& p, const Bufs& f, cudaStre
   const GTiles T = gtiles(p.N, p.Q);
   CUtensorMap X, Y, B, C, S, H;
   if (!group_maps(p, f, &X, &Y, &B, &C, &S, &H)) return cudaErrorInvalidValue;
-  const size_t smem = group_smem_bytes(T, p.Q);
+  const size_t smem = group_smem_bytes(T, p.Q, p.hpg);
   cudaError_t e = cudaFuncSetAttribute(chunk_bwd_dbc_group_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -753,7 +805,7 @@ cudaError_t launch_chunk_bwd_group_tc(const Plan& p, const Bufs& f, cudaStream_t
   const GTiles T = gtiles(p.N, p.Q);
   CUtensorMap X, Y, B, C, S, H;
   if (!group_maps(p, f, &X, &Y, &B, &C, &S, &H)) return cudaErrorInvalidValue;
-  const size_t smem = group_smem_bytes(T, p.Q);
+  const size_t smem = group_smem_bytes(T, p.Q, p.hpg);
   cudaError_t e = cudaFuncSetAttribute(chunk_bwd_group_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

@@ -19,15 +19,20 @@
 // Decomposition.  A tile is (row b, head h, a block of 1024 consecutive state
 // elements, a segment of kSpSeg consecutive chunks).  Each thread owns 4
 // consecutive elements (one float4, coalesced across the CTA) and scans its
-// segment sequentially -- work-efficient, the loads do not depend on the
-// carry and are all issued up front.  Segments are joined by decoupled
-// lookback: a tile publishes its aggregate pair (the product of the decays, the
-// locally scanned state) as soon as it has it, then walks back over its
-// predecessors, folding aggregates until it meets a published inclusive
-// prefix.  Tiles take their index from an atomic ticket, so every tile a
-// tile waits on is already resident: the waits always end.  Each wait is also
-// bounded in time; on expiry the tile records a timeout in the status word
-// and continues with a zero prefix instead of hanging.
+// segment sequentially -- work-efficient; the loads do not depend on the
+// carry and are all issued up front.  Segments are joined by a look-back
+// over published per-segment aggregates (the product of the decays, the
+// locally scanned state), decoupled from the predecessors' own joins: every
+// kSpSpan-th segment is a checkpoint that publishes its inclusive prefix;
+// any other segment publishes its aggregate as soon as its local scan is
+// done and then folds, in chunk order, the aggregates back to the nearest
+// checkpoint before it.  The fold order is fixed, so the result does not
+// depend on which predecessor happened to finish first: every run gives the
+// same bits.  Only checkpoints wait on a predecessor's join, so the serial
+// chain is nseg / kSpSpan long.  Tiles take their index from an atomic
+// ticket, so every tile a tile waits on is already resident: the waits always
+// end.  Each wait is also bounded in time; on expiry the tile records a
+// timeout in the status word and continues instead of hanging.
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -55,6 +60,7 @@ __device__ __forceinline__ float4 fma4(float a, float4 x, float4 y) {
 }
 
 enum : int { kFlagNone = 0, kFlagAggregate = 1, kFlagPrefix = 2 };
+constexpr int kSpSpan = 8;  // segments from one checkpoint to the next
 
 // Public state tensors are (b, H, P, N); the chunk-state layout is (N, P):
 // the 4 consecutive elements e..e+3 (same n, headdim p..p+3) of a thread map
@@ -88,11 +94,15 @@ __device__ __forceinline__ void store4(__nv_bfloat16* dst, float4 v) {
 // those fp32 carry-in states: one partial per (chunk, element block), folded
 // over the block's warps in a fixed order.
 template <bool kBwd, bool kKeepF32, typename TOut>
-__global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs f) {
-  __shared__ int s_ticket, s_flag;
+__global__ void __launch_bounds__(kSpThreads, kBwd ? 2 : 4) state_passing_kernel(Plan p, Bufs f) {
+  __shared__ int s_ticket, s_timeout;
+  __shared__ float s_A[kSpSpan];  // decay products of the folded segments
   __shared__ float s_da[kSpSeg][kSpThreads / 32];
   int* flags = kBwd ? f.flags_bwd : f.flags_fwd;
-  if (threadIdx.x == 0) s_ticket = atomicAdd(kBwd ? &f.hdr->ticket_bwd : &f.hdr->ticket_fwd, 1);
+  if (threadIdx.x == 0) {
+    s_ticket = atomicAdd(kBwd ? &f.hdr->ticket_bwd : &f.hdr->ticket_fwd, 1);
+    s_timeout = 0;
+  }
   __syncthreads();
   const int ticket = s_ticket;
   const int seg = ticket / p.sp_chains;
@@ -106,9 +116,11 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
   const float* achunk = f.achunk + bh * p.nc;
   const float* in = kBwd ? f.dHl : f.S;  // forward: chunk states; backward: dHloc
   TOut* out = static_cast<TOut*>(kBwd ? f.dS : f.Hin);
-  const size_t lb_slot = ((size_t)chain * p.sp_nseg + seg) * kSpElems + threadIdx.x * 4;
   const unsigned long long limit =
       (p.flags & SSD_TEST_DROP_SCAN_PUBLISH) ? kTestWaitLimitNs : kWaitLimitNs;
+  auto chunk_of = [&](int k) { return kBwd ? p.nc - 1 - k : k; };  // k-th chunk in scan order
+  auto slot_of = [&](int sg) { return ((size_t)chain * p.sp_nseg + sg) * kSpElems + threadIdx.x * 4; };
+  auto state_off = [&](int k) { return ((size_t)bh * p.nc + chunk_of(k0 + k)) * p.PN + e; };
 
   // 1) local scan of the segment from a zero state; v[k] becomes the value
   //    entering chunk k, dprod[k] the product of the decays before chunk k.
@@ -117,18 +129,22 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
 #pragma unroll
   for (int k = 0; k < kSpSeg; ++k) {
     v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (k < nk && active) {
-      const int c = kBwd ? p.nc - 1 - (k0 + k) : k0 + k;
-      v[k] = __ldcs(reinterpret_cast<const float4*>(in + ((size_t)bh * p.nc + c) * p.PN + e));
-    }
+    if (k < nk && active) v[k] = __ldcs(reinterpret_cast<const float4*>(in + state_off(k)));
+  }
+  // backward: the fp32 carry-in states of the segment's chunks, for dL/da_c
+  // at the end (loaded now, so that their latency hides under the join)
+  float4 hv[kBwd ? kSpSeg : 1];
+#pragma unroll
+  for (int k = 0; k < (kBwd ? kSpSeg : 0); ++k) {
+    hv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (k < nk && active) hv[k] = __ldcs(reinterpret_cast<const float4*>(f.S + state_off(k)));
   }
   float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
   float aprod = 1.0f;
 #pragma unroll
   for (int k = 0; k < kSpSeg; ++k) {
     if (k < nk) {
-      const int c = kBwd ? p.nc - 1 - (k0 + k) : k0 + k;
-      const float a = __ldg(achunk + c);
+      const float a = __ldg(achunk + chunk_of(k0 + k));
       const float4 x = v[k];
       v[k] = run;
       dprod[k] = aprod;
@@ -138,77 +154,59 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
   }
 
   // 2) join with the predecessors
+  const bool is_check = seg % kSpSpan == 0;
+  const bool drop = (p.flags & SSD_TEST_DROP_SCAN_PUBLISH) && seg == 0 && chain == 0;
   float4 prefix = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!is_check && seg + 1 < p.sp_nseg) {  // publish the aggregate at once
+    if (active) __stcg(reinterpret_cast<float4*>(f.agg + slot_of(seg)), run);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) st_release(flags + (size_t)chain * p.sp_nseg + seg, kFlagAggregate);
+  }
   if (seg == 0) {
     const float* start = kBwd ? f.dfinal : f.init;
     if (start != nullptr && active) prefix = load_public(start + bh * p.PN, e, p.P, p.N);
   } else {
-    if (active) __stcg(reinterpret_cast<float4*>(f.agg + lb_slot), run);
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) st_release(flags + (size_t)chain * p.sp_nseg + seg, kFlagAggregate);
-    float acc_a = 1.0f;
-    float4 acc_v = make_float4(0.f, 0.f, 0.f, 0.f);
-    int sp = seg - 1;
-    bool joined = false;
-    while (sp >= 0) {
-      if (threadIdx.x == 0) {
-        const int* fp = flags + (size_t)chain * p.sp_nseg + sp;
-        int fl = ld_acquire(fp);
-        if (fl == kFlagNone) {
-          const unsigned long long t_start = global_ns();
-          const long long c_start = clock64();
-          unsigned polls = 0;
-          while ((fl = ld_acquire(fp)) == kFlagNone) {
-            if (global_ns() - t_start > limit || clock64() - c_start > 2 * (long long)limit ||
-                ++polls > (1u << 24)) {
-              atomicOr(&f.hdr->status, kDevTimeout);
-              fl = -1;
-              break;
-            }
-            __nanosleep(128);
+    // the nearest checkpoint before this segment, and the segments between
+    const int anchor = is_check ? seg - kSpSpan : (seg / kSpSpan) * kSpSpan;
+    const int nfold = seg - anchor - 1;
+    if (threadIdx.x <= nfold) {  // thread t waits for segment anchor + t
+      const int* fp = flags + (size_t)chain * p.sp_nseg + anchor + threadIdx.x;
+      if (ld_acquire(fp) == kFlagNone) {
+        const unsigned long long t_start = global_ns();
+        const long long c_start = clock64();
+        unsigned polls = 0;
+        while (ld_acquire(fp) == kFlagNone) {
+          if (global_ns() - t_start > limit || clock64() - c_start > 2 * (long long)limit ||
+              ++polls > (1u << 24)) {
+            atomicOr(&f.hdr->status, kDevTimeout);
+            s_timeout = 1;
+            break;
           }
+          __nanosleep(128);
         }
-        __threadfence();
-        s_flag = fl;
       }
-      __syncthreads();
-      const int fl = s_flag;
-      __syncthreads();
-      if (fl < 0) break;  // timed out: continue from what has been folded so far
-      const size_t slot = ((size_t)chain * p.sp_nseg + sp) * kSpElems + threadIdx.x * 4;
-      if (fl == kFlagPrefix) {
-        float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (active) pv = __ldcg(reinterpret_cast<const float4*>(f.incl + slot));
-        prefix = fma4(acc_a, pv, acc_v);
-        joined = true;
-        break;
-      }
-      // aggregate of segment sp: fold it under the spans already folded
-      float4 av = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (active) av = __ldcg(reinterpret_cast<const float4*>(f.agg + slot));
-      float a_sp = 1.0f;
-      const int ks = sp * kSpSeg, kn = min(kSpSeg, p.nc - ks);
-      for (int k = 0; k < kn; ++k) a_sp *= __ldg(achunk + (kBwd ? p.nc - 1 - (ks + k) : ks + k));
-      acc_v = fma4(acc_a, av, acc_v);
-      acc_a *= a_sp;
-      --sp;
+      __threadfence();
     }
-    if (!joined) {
-      if (sp < 0) {  // walked back to the chain start
-        const float* start = kBwd ? f.dfinal : f.init;
-        float4 sv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (start != nullptr && active) sv = load_public(start + bh * p.PN, e, p.P, p.N);
-        prefix = fma4(acc_a, sv, acc_v);
-      } else {
-        prefix = acc_v;  // timed out
+    if (threadIdx.x < nfold) {  // decay product of segment anchor + 1 + t, in chunk order
+      const int sg = anchor + 1 + threadIdx.x;
+      float a = 1.0f;
+      for (int k = 0; k < kSpSeg; ++k) a *= __ldg(achunk + chunk_of(sg * kSpSeg + k));
+      s_A[threadIdx.x] = a;
+    }
+    __syncthreads();
+    if (active && !s_timeout) {
+      prefix = __ldcg(reinterpret_cast<const float4*>(f.incl + slot_of(anchor)));
+#pragma unroll 1
+      for (int t = 0; t < nfold; ++t) {
+        const float4 bk = __ldcg(reinterpret_cast<const float4*>(f.agg + slot_of(anchor + 1 + t)));
+        prefix = fma4(s_A[t], prefix, bk);
       }
     }
   }
   const float4 incl = fma4(aprod, prefix, run);
-  const bool drop = (p.flags & SSD_TEST_DROP_SCAN_PUBLISH) && seg == 0 && chain == 0;
-  if (seg + 1 < p.sp_nseg && !drop) {
-    if (active) __stcg(reinterpret_cast<float4*>(f.incl + lb_slot), incl);
+  if (is_check && seg + 1 < p.sp_nseg && !drop) {  // checkpoints publish their inclusive prefix
+    if (active) __stcg(reinterpret_cast<float4*>(f.incl + slot_of(seg)), incl);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) st_release(flags + (size_t)chain * p.sp_nseg + seg, kFlagPrefix);
@@ -218,19 +216,15 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
 #pragma unroll
   for (int k = 0; k < kSpSeg; ++k) {
     if (k < nk) {
-      const int c = kBwd ? p.nc - 1 - (k0 + k) : k0 + k;
-      const size_t off = ((size_t)bh * p.nc + c) * p.PN + e;
+      const size_t off = state_off(k);
       const float4 val = fma4(dprod[k], prefix, v[k]);
       if (active) {
         store4(out + off, val);
         if (kKeepF32) *reinterpret_cast<float4*>(f.S + off) = val;
       }
       if (kBwd) {
-        float d = 0.0f;
-        if (active) {
-          const float4 hv = __ldcs(reinterpret_cast<const float4*>(f.S + off));
-          d = val.x * hv.x + val.y * hv.y + val.z * hv.z + val.w * hv.w;
-        }
+        const float4 h4 = hv[k];
+        float d = val.x * h4.x + val.y * h4.y + val.z * h4.z + val.w * h4.w;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
         if ((threadIdx.x & 31) == 0) s_da[k][threadIdx.x >> 5] = d;
@@ -241,10 +235,9 @@ __global__ void __launch_bounds__(kSpThreads) state_passing_kernel(Plan p, Bufs 
     __syncthreads();
     if (threadIdx.x < nk) {
       const int k = threadIdx.x;
-      const int c = p.nc - 1 - (k0 + k);
       float d = 0.0f;
       for (int w = 0; w < kSpThreads / 32; ++w) d += s_da[k][w];
-      f.dapart[((size_t)bh * p.nc + c) * p.sp_neblk + eblk] = d;
+      f.dapart[((size_t)bh * p.nc + chunk_of(k0 + k)) * p.sp_neblk + eblk] = d;
     }
   }
   if (active) {

@@ -17,7 +17,7 @@ enum : int { kDevTimeout = 1 };
 // (kSpThreads threads x 4 floats) over kSpSeg consecutive chunks.
 constexpr int kSpThreads = 256;
 constexpr int kSpElems = kSpThreads * 4;
-constexpr int kSpSeg = 8;
+constexpr int kSpSeg = 16;
 
 // Workspace header (first 256 bytes): device status word, then the tile
 // tickets of the forward and backward state-passing scans.

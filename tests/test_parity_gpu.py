@@ -59,6 +59,12 @@ SMALL = {
                                     ngroups=2, chunk=128, dtype="bf16"),
     "bf16_many_chunks": dict(batch=1, seqlen=64 * 40 + 5, nheads=2, headdim=64, dstate=16,
                              ngroups=1, chunk=64, dtype="bf16", init=True, dfinal=True),
+    # 201 chunks: 26 scan segments of 8 chunks, joined across 4 checkpoint spans
+    "bf16_many_segments": dict(batch=2, seqlen=64 * 200 + 7, nheads=2, headdim=64, dstate=32,
+                               ngroups=1, chunk=64, dtype="bf16", init=True, dfinal=True,
+                               seq_lengths=[5000, 1, 7806]),
+    "fp32_many_segments": dict(batch=1, seqlen=32 * 150, nheads=2, headdim=16, dstate=16,
+                               ngroups=1, chunk=32, dtype="f32", init=True, dfinal=True),
 }
 
 
@@ -90,6 +96,21 @@ def test_backward_is_bitwise_deterministic():
     b = dev.results()
     for k in a:
         assert torch.equal(a[k], b[k]), k
+
+
+def test_scan_across_checkpoints_is_bitwise_deterministic():
+    """The scan's look-back folds the published segment aggregates in a fixed
+    order, so repeated calls give the same bits whichever tiles finish first."""
+    inp = make_inputs(seed=11, **SMALL["bf16_many_segments"])
+    dev, a = run_device(inp)
+    for _ in range(3):
+        dev.fwd()
+        dev.bwd()
+        torch.cuda.synchronize()
+        assert dev.device_status() == 0
+        b = dev.results()
+        for k in a:
+            assert torch.equal(a[k], b[k]), k
 
 
 def test_scan_wait_timeout_is_reported_not_hung():
