@@ -34,7 +34,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) dt_cumsum_kernel(Plan p, Bufs f) {
   // Zero this call's scan flags and tickets and the status word.
   {
-    const long long nflags = (long long)p.sp_chains * p.sp_nseg;
+    const long long nflags = (long long)p.sp_chains * p.sp_nslot;
     const long long nthr = (long long)gridDim.x * gridDim.y * gridDim.z * blockDim.x;
     long long gid = (((long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) *
                         blockDim.x + threadIdx.x;

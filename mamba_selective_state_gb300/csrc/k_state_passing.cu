@@ -17,12 +17,15 @@
 // The backward is the same scan run over the chunks in reverse order.
 //
 // Decomposition.  A tile is (row b, head h, a block of 1024 consecutive state
-// elements, a segment of kSpSeg consecutive chunks).  Each thread owns 4
-// consecutive elements (one float4, coalesced across the CTA) and scans its
-// segment sequentially -- work-efficient; the loads do not depend on the
-// carry and are all issued up front.  Segments are joined by a look-back
-// over published per-segment aggregates (the product of the decays, the
-// locally scanned state), decoupled from the predecessors' own joins: every
+// elements, a segment of consecutive chunks: 16 forward, 8 in reverse).  One
+// thread issues bulk asynchronous copies of the segment's chunk blocks (4 KB
+// each; in reverse also the fp32 carry-in states) into shared memory, so the
+// whole segment is in flight at once without holding registers; each thread
+// then owns 4 consecutive elements (one float4, conflict-free in shared
+// memory, coalesced in global memory) and scans the segment sequentially in
+// place -- work-efficient.  Segments are joined by a look-back over
+// published per-segment aggregates (the product of the decays, the locally
+// scanned state), decoupled from the predecessors' own joins: every
 // kSpSpan-th segment is a checkpoint that publishes its inclusive prefix;
 // any other segment publishes its aggregate as soon as its local scan is
 // done and then folds, in chunk order, the aggregates back to the nearest
@@ -34,6 +37,7 @@
 // end.  Each wait is also bounded in time; on expiry the tile records a
 // timeout in the status word and continues instead of hanging.
 #include "ssd_internal.cuh"
+#include "tc_common.cuh"
 
 namespace ssd {
 
@@ -61,6 +65,7 @@ __device__ __forceinline__ float4 fma4(float a, float4 x, float4 y) {
 
 enum : int { kFlagNone = 0, kFlagAggregate = 1, kFlagPrefix = 2 };
 constexpr int kSpSpan = 8;  // segments from one checkpoint to the next
+static_assert(kSpSpan <= 32 && kSpThreads >= 96, "look-back waits use warp 1, decays warp 2");
 
 // Public state tensors are (b, H, P, N); the chunk-state layout is (N, P):
 // the 4 consecutive elements e..e+3 (same n, headdim p..p+3) of a thread map
@@ -89,19 +94,30 @@ __device__ __forceinline__ void store4(__nv_bfloat16* dst, float4 v) {
 // Outputs (carry-in states forward, dS backward) are written in the problem
 // dtype TOut; the scan itself runs in fp32.
 // kKeepF32 (forward only): also store the fp32 carry-in states over the chunk
-// states just read (each element is read before it is written, by the same
-// thread).  The backward also forms dL/da_c = <dS_c, H_in[c]> in fp32 from
-// those fp32 carry-in states: one partial per (chunk, element block), folded
-// over the block's warps in a fixed order.
+// states just read.  The backward also forms dL/da_c = <dS_c, H_in[c]> in
+// fp32 from those fp32 carry-in states: one partial per (chunk, element
+// block), folded over the block's warps in a fixed order.
+template <bool kBwd>
+__host__ __device__ constexpr int sp_seg() { return kBwd ? kSpSegB : kSpSegF; }
+template <bool kBwd>
+__host__ __device__ constexpr size_t sp_smem_bytes() { return (size_t)sp_seg<kBwd>() * kSpElems * 4 * (kBwd ? 2 : 1); }
+
 template <bool kBwd, bool kKeepF32, typename TOut>
-__global__ void __launch_bounds__(kSpThreads, kBwd ? 2 : 4) state_passing_kernel(Plan p, Bufs f) {
+__global__ void __launch_bounds__(kSpThreads, 3) state_passing_kernel(Plan p, Bufs f) {
+  constexpr int kSeg = sp_seg<kBwd>();
+  extern __shared__ __align__(128) float s_buf[];  // [kSeg][kSpElems] inputs; reverse: then [kSeg][kSpElems] H_in
+  __shared__ __align__(8) uint64_t s_bar;
   __shared__ int s_ticket, s_timeout;
   __shared__ float s_A[kSpSpan];  // decay products of the folded segments
-  __shared__ float s_da[kSpSeg][kSpThreads / 32];
+  __shared__ float s_a[kSeg];     // decays of this segment's chunks, in scan order
+  __shared__ float s_da[kSeg][kSpThreads / 32];
   int* flags = kBwd ? f.flags_bwd : f.flags_fwd;
+  const int nseg = kBwd ? p.sp_nseg_b : p.sp_nseg;
   if (threadIdx.x == 0) {
     s_ticket = atomicAdd(kBwd ? &f.hdr->ticket_bwd : &f.hdr->ticket_fwd, 1);
     s_timeout = 0;
+    tc::mbar_init(&s_bar, 1);
+    tc::mbar_fence_init();
   }
   __syncthreads();
   const int ticket = s_ticket;
@@ -109,47 +125,51 @@ __global__ void __launch_bounds__(kSpThreads, kBwd ? 2 : 4) state_passing_kernel
   const int chain = ticket - seg * p.sp_chains;
   const int eblk = chain % p.sp_neblk;
   const long long bh = chain / p.sp_neblk;  // bi * H + h
-  const int e = eblk * kSpElems + threadIdx.x * 4;
+  const int e0 = eblk * kSpElems;
+  const int ne = min(kSpElems, p.PN - e0);  // elements of this block (a multiple of 256)
+  const int e = e0 + threadIdx.x * 4;
   const bool active = e < p.PN;
-  const int k0 = seg * kSpSeg;
-  const int nk = min(kSpSeg, p.nc - k0);
+  const int k0 = seg * kSeg;
+  const int nk = min(kSeg, p.nc - k0);
   const float* achunk = f.achunk + bh * p.nc;
   const float* in = kBwd ? f.dHl : f.S;  // forward: chunk states; backward: dHloc
   TOut* out = static_cast<TOut*>(kBwd ? f.dS : f.Hin);
   const unsigned long long limit =
       (p.flags & SSD_TEST_DROP_SCAN_PUBLISH) ? kTestWaitLimitNs : kWaitLimitNs;
   auto chunk_of = [&](int k) { return kBwd ? p.nc - 1 - k : k; };  // k-th chunk in scan order
-  auto slot_of = [&](int sg) { return ((size_t)chain * p.sp_nseg + sg) * kSpElems + threadIdx.x * 4; };
-  auto state_off = [&](int k) { return ((size_t)bh * p.nc + chunk_of(k0 + k)) * p.PN + e; };
+  auto slot_of = [&](int sg) { return ((size_t)chain * nseg + sg) * kSpElems + threadIdx.x * 4; };
+  auto state_off = [&](int k) { return ((size_t)bh * p.nc + chunk_of(k0 + k)) * p.PN + e0; };
 
-  // 1) local scan of the segment from a zero state; v[k] becomes the value
-  //    entering chunk k, dprod[k] the product of the decays before chunk k.
-  float4 v[kSpSeg];
-  float dprod[kSpSeg];
-#pragma unroll
-  for (int k = 0; k < kSpSeg; ++k) {
-    v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (k < nk && active) v[k] = __ldcs(reinterpret_cast<const float4*>(in + state_off(k)));
+  // 1) the segment's blocks into shared memory; then the segment's aggregate
+  //    (a local scan from a zero state; it is redone in step 3, where the
+  //    value entering each chunk is needed, instead of being stored)
+  if (threadIdx.x == 0) {
+    const uint32_t bytes = (uint32_t)ne * 4u;
+    tc::mbar_expect_tx(&s_bar, bytes * nk * (kBwd ? 2u : 1u));
+    for (int k = 0; k < nk; ++k) {
+      tc::bulk_load(s_buf + k * kSpElems, in + state_off(k), bytes, &s_bar);
+      if (kBwd) tc::bulk_load(s_buf + (kSeg + k) * kSpElems, f.S + state_off(k), bytes, &s_bar);
+    }
   }
-  // backward: the fp32 carry-in states of the segment's chunks, for dL/da_c
-  // at the end (loaded now, so that their latency hides under the join)
-  float4 hv[kBwd ? kSpSeg : 1];
-#pragma unroll
-  for (int k = 0; k < (kBwd ? kSpSeg : 0); ++k) {
-    hv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (k < nk && active) hv[k] = __ldcs(reinterpret_cast<const float4*>(f.S + state_off(k)));
-  }
+  if (threadIdx.x < nk) s_a[threadIdx.x] = __ldg(achunk + chunk_of(k0 + threadIdx.x));
+  __syncthreads();
+  if (!tc::mbar_wait(&s_bar, 0)) atomicOr(&f.hdr->status, kDevTimeout);
+  float4* vb = reinterpret_cast<float4*>(s_buf) + threadIdx.x;  // block k at vb[k * kSpThreads]
   float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
   float aprod = 1.0f;
+  constexpr int kBatch = kSeg < 8 ? kSeg : 8;  // loads issued together: only the FMA chain is serial
 #pragma unroll
-  for (int k = 0; k < kSpSeg; ++k) {
-    if (k < nk) {
-      const float a = __ldg(achunk + chunk_of(k0 + k));
-      const float4 x = v[k];
-      v[k] = run;
-      dprod[k] = aprod;
-      run = fma4(a, run, x);
-      aprod *= a;
+  for (int kb = 0; kb < kSeg; kb += kBatch) {
+    float4 x[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+      x[k] = (kb + k < nk && active) ? vb[(kb + k) * kSpThreads] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      if (kb + k < nk) {
+        run = fma4(s_a[kb + k], run, x[k]);
+        aprod *= s_a[kb + k];
+      }
     }
   }
 
@@ -157,11 +177,10 @@ __global__ void __launch_bounds__(kSpThreads, kBwd ? 2 : 4) state_passing_kernel
   const bool is_check = seg % kSpSpan == 0;
   const bool drop = (p.flags & SSD_TEST_DROP_SCAN_PUBLISH) && seg == 0 && chain == 0;
   float4 prefix = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (!is_check && seg + 1 < p.sp_nseg) {  // publish the aggregate at once
+  if (!is_check && seg + 1 < nseg) {  // publish the aggregate at once
     if (active) __stcg(reinterpret_cast<float4*>(f.agg + slot_of(seg)), run);
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) st_release(flags + (size_t)chain * p.sp_nseg + seg, kFlagAggregate);
+    __syncthreads();  // every thread's part is written; one release (cumulative) publishes them all
+    if (threadIdx.x == 0) st_release(flags + (size_t)chain * nseg + seg, kFlagAggregate);
   }
   if (seg == 0) {
     const float* start = kBwd ? f.dfinal : f.init;
@@ -170,8 +189,11 @@ __global__ void __launch_bounds__(kSpThreads, kBwd ? 2 : 4) state_passing_kernel
     // the nearest checkpoint before this segment, and the segments between
     const int anchor = is_check ? seg - kSpSpan : (seg / kSpSpan) * kSpSpan;
     const int nfold = seg - anchor - 1;
-    if (threadIdx.x <= nfold) {  // thread t waits for segment anchor + t
-      const int* fp = flags + (size_t)chain * p.sp_nseg + anchor + threadIdx.x;
+    // lane t of warp 1 waits for segment anchor + t (warp 0 may still be
+    // releasing this tile's aggregate; warp 2 reads the decays meanwhile)
+    const int tw = (int)threadIdx.x - 32;
+    if (tw >= 0 && tw <= nfold) {
+      const int* fp = flags + (size_t)chain * nseg + anchor + tw;
       if (ld_acquire(fp) == kFlagNone) {
         const unsigned long long t_start = global_ns();
         const long long c_start = clock64();
@@ -186,50 +208,65 @@ __global__ void __launch_bounds__(kSpThreads, kBwd ? 2 : 4) state_passing_kernel
           __nanosleep(128);
         }
       }
-      __threadfence();
     }
-    if (threadIdx.x < nfold) {  // decay product of segment anchor + 1 + t, in chunk order
-      const int sg = anchor + 1 + threadIdx.x;
+    const int ta = (int)threadIdx.x - 64;
+    if (ta >= 0 && ta < nfold) {  // decay product of segment anchor + 1 + t, in chunk order
+      const int sg = anchor + 1 + ta;
       float a = 1.0f;
-      for (int k = 0; k < kSpSeg; ++k) a *= __ldg(achunk + chunk_of(sg * kSpSeg + k));
-      s_A[threadIdx.x] = a;
+      for (int k = 0; k < kSeg; ++k) a *= __ldg(achunk + chunk_of(sg * kSeg + k));
+      s_A[ta] = a;
     }
     __syncthreads();
-    if (active && !s_timeout) {
+    if (active && !s_timeout) {  // every load first, then the fold in chunk order
       prefix = __ldcg(reinterpret_cast<const float4*>(f.incl + slot_of(anchor)));
-#pragma unroll 1
-      for (int t = 0; t < nfold; ++t) {
-        const float4 bk = __ldcg(reinterpret_cast<const float4*>(f.agg + slot_of(anchor + 1 + t)));
-        prefix = fma4(s_A[t], prefix, bk);
-      }
+      float4 bk[kSpSpan - 1];
+#pragma unroll
+      for (int t = 0; t < kSpSpan - 1; ++t)
+        if (t < nfold) bk[t] = __ldcg(reinterpret_cast<const float4*>(f.agg + slot_of(anchor + 1 + t)));
+#pragma unroll
+      for (int t = 0; t < kSpSpan - 1; ++t)
+        if (t < nfold) prefix = fma4(s_A[t], prefix, bk[t]);
     }
   }
   const float4 incl = fma4(aprod, prefix, run);
-  if (is_check && seg + 1 < p.sp_nseg && !drop) {  // checkpoints publish their inclusive prefix
+  if (is_check && seg + 1 < nseg && !drop) {  // checkpoints publish their inclusive prefix
     if (active) __stcg(reinterpret_cast<float4*>(f.incl + slot_of(seg)), incl);
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) st_release(flags + (size_t)chain * p.sp_nseg + seg, kFlagPrefix);
+    __syncthreads();  // every thread's part is written; one release (cumulative) publishes them all
+    if (threadIdx.x == 0) st_release(flags + (size_t)chain * nseg + seg, kFlagPrefix);
   }
 
   // 3) carry-in values of the segment's chunks, and the end of the chain
+  float dp = 1.0f;  // product of the decays before chunk k (same order as aprod)
+  float4 loc = make_float4(0.f, 0.f, 0.f, 0.f);  // the local scan again: value entering chunk k
 #pragma unroll
-  for (int k = 0; k < kSpSeg; ++k) {
-    if (k < nk) {
-      const size_t off = state_off(k);
-      const float4 val = fma4(dprod[k], prefix, v[k]);
-      if (active) {
-        store4(out + off, val);
-        if (kKeepF32) *reinterpret_cast<float4*>(f.S + off) = val;
-      }
-      if (kBwd) {
-        const float4 h4 = hv[k];
-        float d = val.x * h4.x + val.y * h4.y + val.z * h4.z + val.w * h4.w;
+  for (int kb = 0; kb < kSeg; kb += kBatch) {
+   float4 x[kBatch];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-        if ((threadIdx.x & 31) == 0) s_da[k][threadIdx.x >> 5] = d;
-      }
+   for (int k2 = 0; k2 < kBatch; ++k2)
+     x[k2] = (kb + k2 < nk && active) ? vb[(kb + k2) * kSpThreads] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+   for (int k2 = 0; k2 < kBatch; ++k2) {
+    const int k = kb + k2;
+    if (k >= nk) break;
+    const size_t off = state_off(k) + threadIdx.x * 4;
+    const float4 val = fma4(dp, prefix, loc);
+    loc = fma4(s_a[k], loc, x[k2]);
+    dp *= s_a[k];
+    if (active) {
+      store4(out + off, val);
+      if (kKeepF32) __stcs(reinterpret_cast<float4*>(f.S + off), val);
     }
+    if (kBwd) {
+      float d = 0.0f;
+      if (active) {
+        const float4 h4 = vb[(kSeg + k) * kSpThreads];
+        d = val.x * h4.x + val.y * h4.y + val.z * h4.z + val.w * h4.w;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      if ((threadIdx.x & 31) == 0) s_da[k][threadIdx.x >> 5] = d;
+    }
+   }
   }
   if (kBwd) {
     __syncthreads();
@@ -241,30 +278,32 @@ __global__ void __launch_bounds__(kSpThreads, kBwd ? 2 : 4) state_passing_kernel
     }
   }
   if (active) {
-    if (seg == p.sp_nseg - 1) {
+    if (seg == nseg - 1) {
       float* fin = kBwd ? f.dinit : f.final_states;
       if (fin != nullptr) store_public(fin + bh * p.PN, e, p.P, p.N, incl);
     }
   }
 }
 
+template <bool kBwd, bool kKeepF32, typename TOut>
+cudaError_t launch_sp(const Plan& p, const Bufs& f, cudaStream_t s) {
+  const unsigned tiles = (unsigned)p.sp_chains * (kBwd ? p.sp_nseg_b : p.sp_nseg);
+  auto kern = state_passing_kernel<kBwd, kKeepF32, TOut>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sp_smem_bytes<kBwd>());
+  if (e != cudaSuccess) return e;
+  kern<<<tiles, kSpThreads, sp_smem_bytes<kBwd>(), s>>>(p, f);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_state_passing(const Plan& p, const Bufs& f, bool backward, bool keep_f32, cudaStream_t s) {
-  const unsigned tiles = (unsigned)p.sp_chains * p.sp_nseg;
   set_kernel_name(backward ? "state_passing_bwd" : (keep_f32 ? "state_passing_fwd_keep" : "state_passing_fwd"));
   const bool bf = p.dtype == SSD_BF16;
-  if (backward) {
-    if (bf) state_passing_kernel<true, false, __nv_bfloat16><<<tiles, kSpThreads, 0, s>>>(p, f);
-    else state_passing_kernel<true, false, float><<<tiles, kSpThreads, 0, s>>>(p, f);
-  } else if (keep_f32) {
-    if (bf) state_passing_kernel<false, true, __nv_bfloat16><<<tiles, kSpThreads, 0, s>>>(p, f);
-    else state_passing_kernel<false, true, float><<<tiles, kSpThreads, 0, s>>>(p, f);
-  } else {
-    if (bf) state_passing_kernel<false, false, __nv_bfloat16><<<tiles, kSpThreads, 0, s>>>(p, f);
-    else state_passing_kernel<false, false, float><<<tiles, kSpThreads, 0, s>>>(p, f);
-  }
-  return cudaGetLastError();
+  if (backward) return bf ? launch_sp<true, false, __nv_bfloat16>(p, f, s) : launch_sp<true, false, float>(p, f, s);
+  if (keep_f32) return bf ? launch_sp<false, true, __nv_bfloat16>(p, f, s) : launch_sp<false, true, float>(p, f, s);
+  return bf ? launch_sp<false, false, __nv_bfloat16>(p, f, s) : launch_sp<false, false, float>(p, f, s);
 }
 
 }  // namespace ssd

@@ -74,7 +74,9 @@ int make_plan(const ssd_problem* pr, Plan* p) {
   p->flags = pr->flags;
   p->Lp = (long long)p->nc * p->Q;
   p->sp_neblk = (p->PN + kSpElems - 1) / kSpElems;
-  p->sp_nseg = (p->nc + kSpSeg - 1) / kSpSeg;
+  p->sp_nseg = (p->nc + kSpSegF - 1) / kSpSegF;
+  p->sp_nseg_b = (p->nc + kSpSegB - 1) / kSpSegB;
+  p->sp_nslot = p->sp_nseg > p->sp_nseg_b ? p->sp_nseg : p->sp_nseg_b;
   p->sp_chains = p->b * p->H * p->sp_neblk;
   // per-chunk partial slots of the chunk-backward kernel: one per chunk on
   // the tensor-core path, one per 32-token block on the CUDA-core path
@@ -94,7 +96,7 @@ int make_plan(const ssd_problem* pr, Plan* p) {
   p->off_achunk = take(bh * p->nc * f4);
   p->off_S = take(states);
   p->off_Hin = take(states / 4 * (p->dtype == SSD_BF16 ? 2 : 4));
-  const size_t lb = (size_t)p->sp_chains * p->sp_nseg;
+  const size_t lb = (size_t)p->sp_chains * p->sp_nslot;
   p->off_agg = take(lb * kSpElems * f4);
   p->off_incl = take(lb * kSpElems * f4);
   p->off_flags_fwd = take(lb * sizeof(int));

@@ -14,10 +14,13 @@ namespace ssd {
 enum : int { kDevTimeout = 1 };
 
 // State-passing scan tiling: one CTA scans kSpElems consecutive state elements
-// (kSpThreads threads x 4 floats) over kSpSeg consecutive chunks.
+// (kSpThreads threads x 4 floats) over a segment of consecutive chunks:
+// kSpSegF in the forward scan, kSpSegB in the reverse scan (which also stages
+// the fp32 carry-in states, so its segments are half as long).
 constexpr int kSpThreads = 256;
 constexpr int kSpElems = kSpThreads * 4;
-constexpr int kSpSeg = 16;
+constexpr int kSpSegF = 16;
+constexpr int kSpSegB = 8;
 
 // Workspace header (first 256 bytes): device status word, then the tile
 // tickets of the forward and backward state-passing scans.
@@ -35,7 +38,7 @@ struct Plan {
   int dtype, flags;
   long long Lp;                          // nc * Q (padded tokens per row)
   // state-passing scan tiling
-  int sp_neblk, sp_nseg, sp_chains;      // chains = b * H * neblk
+  int sp_neblk, sp_nseg, sp_nseg_b, sp_nslot, sp_chains;  // chains = b * H * neblk; nslot = max segments
   // chunk-backward token blocks per chunk
   int cb_ntb;
   // workspace offsets in bytes (0 = absent)
@@ -45,8 +48,8 @@ struct Plan {
   size_t off_S;                          // (b,H,nc,N,P) f32: chunk states; in the backward,
                                          // then the fp32 carry-in states (in place)
   size_t off_Hin;                        // (b,H,nc,N,P) dtype: carry-in states
-  size_t off_agg, off_incl;              // (chains, nseg, kSpElems) f32 each
-  size_t off_flags_fwd, off_flags_bwd;   // (chains, nseg) int32 each
+  size_t off_agg, off_incl;              // (chains, nslot, kSpElems) f32 each
+  size_t off_flags_fwd, off_flags_bwd;   // (chains, nslot) int32 each
   // backward only
   size_t off_dS;                         // (b,H,nc,N,P) dtype: dL/dS_c
   size_t off_dHl;                        // (b,H,nc,N,P) f32: dL/dH_in[c] from the chunk outputs
