@@ -18,6 +18,7 @@ Prints one JSON line (rank 0).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -32,6 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "SSD layer fwd+bwd tokens/s (ms) at b2·L8192 bf16; % of HBM / tensor roofline"
 DEFAULT_WORKLOAD = "b2_L8192_bf16"
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+CSRC_DIR = os.path.join(ROOT, "mamba_selective_state_gb300", "csrc")
 FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
 
 
@@ -77,6 +79,36 @@ def kernel_model(cfg, dtype_bytes):
     layer_io = (tokx + T * H * s + 2 * tokbc + tokx) + (2 * tokx + T * H * s + 2 * tokbc
                                                         + tokx + T * H * s + 2 * tokbc)
     return m, layer_io
+
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# one ncu capture of a b2_L8192_bf16 step (profiles/launches_b2_L8192_bf16.md),
+# keyed by kernel, with the sha1 of the sources the kernel was built from: the
+# figure is reported only while those sources are unchanged and the workload
+# is the one captured, else null.
+NCU_TRAFFIC_WORKLOAD = "b2_L8192_bf16"
+NCU_TRAFFIC = {
+    "chunk_bwd_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.362e+08, "7f59f98c8bca5a2837fba1c528058e77cbeaddbf"),
+    "chunk_bwd_dbc_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.643e+08, "7f59f98c8bca5a2837fba1c528058e77cbeaddbf"),
+    "chunk_scan_tc": (('k_chunk_scan_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.552e+08, "15f2a6d7f2dba4ff8c8611d246280468f23c275f"),
+    "chunk_state_tc": (('k_chunk_state_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.854e+08, "87bc7e3faa1a983969e66df75fbe2c60ba2b67e9"),
+    "chunk_dstate_tc": (('k_chunk_state_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.806e+08, "87bc7e3faa1a983969e66df75fbe2c60ba2b67e9"),
+    "state_passing_fwd": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.98e+08, "2a2abdf015e4bd8d2d9ffef836bbfab7d10feb4f"),
+    "state_passing_fwd_keep": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.337e+08, "2a2abdf015e4bd8d2d9ffef836bbfab7d10feb4f"),
+    "state_passing_bwd": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.533e+08, "2a2abdf015e4bd8d2d9ffef836bbfab7d10feb4f"),
+}
+
+
+def ncu_traffic(kname, workload):
+    ent = NCU_TRAFFIC.get(kname)
+    if ent is None or workload != NCU_TRAFFIC_WORKLOAD:
+        return None
+    files, nbytes, sha = ent
+    h = hashlib.sha1()
+    for fn in files:
+        with open(os.path.join(CSRC_DIR, fn), "rb") as fh:
+            h.update(fh.read())
+    return nbytes if h.hexdigest() == sha else None
 
 
 def base_name(kname):
@@ -226,12 +258,20 @@ class OracleSample:
                 f"every row ({self.full.batch} rows, all {self.full.nheads} heads) of {self.name}")
 
 
-def cpu_baseline(name, target_s=15.0):
+def cpu_baseline(name, target_s=15.0, min_s=10.0):
+    """The oracle on a bounded sample of the workload: a prefix sized to about
+    target_s seconds, repeated (whole workload too small) until at least
+    min_s seconds of CPU work have been timed."""
     smp = OracleSample(name, target_s)
-    secs, threads = smp.run(smp.Lp)
-    tok = smp.full.batch * smp.Lp
+    secs, threads, reps = 0.0, 1, 0
+    while reps == 0 or (secs < min_s and reps < 20):
+        t, threads = smp.run(smp.Lp)
+        secs += t
+        reps += 1
+    tok = smp.full.batch * smp.Lp * reps
+    sample = smp.describe() + (f", run {reps} times" if reps > 1 else "")
     return {"value": tok / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": smp.describe(), "seconds": secs}
+            "sample": sample, "seconds": secs}
 
 
 def run_reference(args, world, rank):
@@ -352,6 +392,7 @@ def run_gpu(args, world, rank, local):
         roof = {"bound": "hbm", "achieved": ach_gbs, "peak": hbm_peak, "unit": "GB/s",
                 "frac": ach_gbs / hbm_peak, "traffic": None, "kernel": dom,
                 "peak_source": f"{src} hbm_gbs"}
+    roof["traffic"] = ncu_traffic(dom, args.workload)
     roof["algorithmic_bytes"] = dm["bytes"]
     roof["algorithmic_flops"] = dm["flops"]
     roof["ms_per_launch"] = kernels[dom]["ms_per_launch"]
