@@ -38,8 +38,8 @@ FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=
 
 
 # ----------------------------------------------------------------------------
-# algorithmic bytes and flops per launch (the per-unit figures, times the units
-# of one launch; the design doc states the same formulas)
+# algorithmic bytes and flops per launch: the compulsory reads and writes of
+# each kernel (per-unit figures times the units of one launch)
 # ----------------------------------------------------------------------------
 def kernel_model(cfg, dtype_bytes):
     b, L, H, P, N, G, Q = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate",
