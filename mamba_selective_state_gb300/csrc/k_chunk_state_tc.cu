@@ -9,7 +9,7 @@
 // a tcgen05.mma with M = 128 = 2 heads x headdim 64 (A = the two x tiles,
 // token-weighted, MN-major), N = d_state (B tile of the group, MN-major) and
 // K = the chunk's tokens, accumulated in fp32 in tensor memory.  Tokens are
-// streamed in stages of 64 by TMA (128-byte swizzle) through a two-stage
+// streamed in stages of 32 by TMA (128-byte swizzle) through a two-stage
 // mbarrier pipeline; the per-token weights are applied to the x rows in
 // shared memory before the MMA reads them.  The epilogue reads the
 // accumulator back with tcgen05.ld and writes S in the (d_state, headdim)
@@ -24,16 +24,16 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStageTok = 64;   // tokens per pipeline stage
+constexpr int kStageTok = 32;   // tokens per pipeline stage (small stages: four CTAs per SM)
 constexpr int kThr = 128;       // 4 warps: one per TMEM lane quadrant
-constexpr uint32_t kABytes = 2 * kStageTok * 128;  // two heads x 64 tokens x 64 bf16
+constexpr uint32_t kABytes = 2 * kStageTok * 128;  // two heads x kStageTok tokens x 64 bf16
 
 __host__ __device__ inline uint32_t round1024(uint32_t v) { return (v + 1023u) & ~1023u; }
 
 struct StateGeom {
   int bw;          // bytes per B row in one box (2 * min(N, 64))
   int nbox;        // boxes along d_state
-  uint32_t box;    // bytes of one B box (64 tokens)
+  uint32_t box;    // bytes of one B box (kStageTok tokens)
   uint32_t stage;  // bytes of one stage (A + B), 1024-aligned
   uint32_t swz;    // descriptor swizzle code of B
   uint32_t ncols;  // TMEM columns
@@ -119,18 +119,22 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(Plan p, Bufs f,
     uint8_t* A = sm + s * G.stage;
     uint8_t* Bt = A + kABytes;
     if (!mbar_wait(&bar[s], ph)) ok = false;
-    {  // row tid of the stacked x tile: head tid/64, token kb*64 + tid%64
-      const int hh = tid >> 6, r = tid & 63;
+    {  // scale the stage's 2 x kStageTok x rows (128 bytes each) by their token weights
+      constexpr int kRowsStage = 2 * kStageTok;
+      constexpr int kPer = kRowsStage >= kThr ? 1 : kThr / kRowsStage;  // threads per row
+      constexpr int kU4 = 8 / kPer;                                     // 16-byte pieces per thread
+      const int row = tid / kPer, part = tid % kPer;
+      const int hh = row / kStageTok, r = row % kStageTok;
       const float wv = w[hh * p.Q + kb * kStageTok + r];
-      uint4* row = reinterpret_cast<uint4*>(A + hh * (kABytes / 2) + r * 128);
+      uint4* rp = reinterpret_cast<uint4*>(A + hh * (kABytes / 2) + r * 128) + part * kU4;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        uint4 v = row[q];
+      for (int q = 0; q < kU4; ++q) {
+        uint4 v = rp[q];
         v.x = scale_bf16x2(v.x, wv);
         v.y = scale_bf16x2(v.y, wv);
         v.z = scale_bf16x2(v.z, wv);
         v.w = scale_bf16x2(v.w, wv);
-        row[q] = v;
+        rp[q] = v;
       }
     }
     fence_async_smem();
