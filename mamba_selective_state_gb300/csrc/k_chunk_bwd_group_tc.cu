@@ -42,7 +42,8 @@ using namespace tc;
 
 constexpr int kRows = 128;
 constexpr int kCompute = 512;        // 16 compute warps: four read each quarter of the TMEM lanes
-constexpr int kThr = kCompute + 32;  // and one control warp that issues the copies and MMAs
+constexpr int kThr = kCompute + 32;   // dB/dC kernel: and one control warp for the copies and MMAs
+constexpr int kThrT = kCompute + 64;  // token kernel: and two control warps (dX; the next head's batch)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kTok = kRows * 128u;  // one (128 tokens x 64) bf16 tile
 
@@ -95,13 +96,13 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ void zero_padding(const GTiles& T, uint8_t* sXb, uint8_t* sYb, uint8_t* sB,
                                              uint8_t* sC, int tid) {
   if (T.rows >= kRows) return;
-  for (int idx = tid; idx < 4 * (kRows - T.rows) * 8; idx += kThr) {
+  for (int idx = tid; idx < 4 * (kRows - T.rows) * 8; idx += blockDim.x) {
     const int which = idx / ((kRows - T.rows) * 8), k = idx % ((kRows - T.rows) * 8);
     uint8_t* base = (which < 2 ? sXb : sYb) + (which & 1) * kTok + T.rows * 128;
     reinterpret_cast<uint4*>(base)[k] = make_uint4(0, 0, 0, 0);
   }
   const int per = (kRows - T.rows) * T.cw / 16;
-  for (int idx = tid; idx < 2 * T.ncb * per; idx += kThr) {
+  for (int idx = tid; idx < 2 * T.ncb * per; idx += blockDim.x) {
     const int blk = idx / per, k = idx % per;
     uint8_t* base = (blk < T.ncb ? sB : sC) + (blk % T.ncb) * T.cblk + T.rows * T.cw;
     reinterpret_cast<uint4*>(base)[k] = make_uint4(0, 0, 0, 0);
@@ -148,7 +149,7 @@ __device__ __forceinline__ void named_sync_compute() {  // the 16 compute warps 
   asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
 }
 
-__global__ void __launch_bounds__(kThr, 1) chunk_bwd_group_tc_kernel(Plan p, Bufs f,
+__global__ void __launch_bounds__(kThrT, 1) chunk_bwd_group_tc_kernel(Plan p, Bufs f,
                                                                     const __grid_constant__ CUtensorMap tmX,
                                                                     const __grid_constant__ CUtensorMap tmY,
                                                                     const __grid_constant__ CUtensorMap tmB,
@@ -217,12 +218,12 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_group_tc_kernel(Plan p, Buf
     if (hpg > 1) issue_xy(1);
     issue_sh(0);
   }
-  for (int t = tid; t < p.Q; t += kThr) sq[t] = t < len ? seg_of(p, f, bi, (long long)t0 + t) : -1;
+  for (int t = tid; t < p.Q; t += kThrT) sq[t] = t < len ? seg_of(p, f, bi, (long long)t0 + t) : -1;
   if (tid < p.Q) {  // scalars of the group's first head into slot 0
     lq[tid] = f.lcs[bh0 * p.Lp + t0 + tid];
     dtq[tid] = f.dte[bh0 * p.Lp + t0 + tid];
   }
-  for (int k = tid; k < hpg; k += kThr) sD[k] = f.D[h_first + k];
+  for (int k = tid; k < hpg; k += kThrT) sD[k] = f.D[h_first + k];
   zero_padding(T, sXb, sYb, sB, sC, tid);  // rows the tensor copies never write
   if (tid == 0) {
     for (int k = 4; k < 7; ++k) mbar_init(&bar[k], 1);
@@ -240,7 +241,10 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_group_tc_kernel(Plan p, Buf
   bool ok = true;
 
   if (ctl) {
-    // ---------------- control warp: one lane issues every copy and MMA ----------------
+    // ---------------- two control warps; lane 0 of each issues ----------------
+    // warp 0: dX = M^T dy of every head.  warp 1: C B^T, batch 1 (dM, dXs, Yc)
+    // of every head, and the tile copies of the heads after the first two.
+    const int cw = (tid - kCompute) >> 5;
     if (lane == 0) {
       const uint32_t id128 = idesc_bf16(128, 128, 0, 0), id64 = idesc_bf16(128, 64, 0, 1);
       const uint32_t id64t = idesc_bf16(128, 64, 1, 1);
@@ -254,52 +258,55 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_group_tc_kernel(Plan p, Buf
       auto mndesc_rows = [&](const uint8_t* t, int ks) {  // MN-major (64 wide), K along rows
         return smem_desc(smem_u32(t) + ks * 16 * 128, 16, 1024, kSwz128);
       };
-      // batch 1 of head hh: dM = dy x^T, dXs = B dS^T (buffer hh&1), Yc = C H^T
-      auto batch1 = [&](int hh) {
-        const int buf = hh & 1;
-        const uint8_t* sX = sXb + buf * kTok;
-        const uint8_t* sY = sYb + buf * kTok;
-        for (int ks = 0; ks < 4; ++ks) mma_bf16(tDM, kdesc_tok(sY, ks), kdesc_tok(sX, ks), id128, ks > 0);
-        for (int ks = 0; ks < p.N / 16; ++ks) {
-          mma_bf16(tDXS + buf * 64, kdesc_c(sB, ks), mndesc_rows(sS, ks), id64, ks > 0);
-          mma_bf16(tYC, kdesc_c(sC, ks), mndesc_rows(sH, ks), id64, ks > 0);
-        }
-        mma_commit(b_b1);
-      };
-      if (!mbar_wait(b_bc, 0)) ok = false;
-      tc_fence_after();
-      for (int ks = 0; ks < p.N / 16; ++ks)  // C B^T (M = i, N = j, K = d_state), once per group
-        mma_bf16(tCB, kdesc_c(sC, ks), kdesc_c(sB, ks), id128, ks > 0);
-      if (!mbar_wait(&b_xy[0], 0)) ok = false;
-      if (!mbar_wait(b_sh, 0)) ok = false;
-      tc_fence_after();
-      batch1(0);  // its commit also covers C B^T
-      for (int hh = 0; hh < hpg; ++hh) {
-        const int buf = hh & 1;
-        if (hh >= 1 && hh + 1 < hpg) {  // x, dy of head hh+1 into the buffer head hh-1 used, once its
-          // epilogue has read them (that epilogue waited for the head's MMAs)
-          if (!mbar_wait(b_ed, (hh - 1) & 1)) ok = false;
-          issue_xy(hh + 1);
-        }
-        if (hh + 1 < hpg) {  // dS, H of head hh+1 once batch 1 of head hh has read them
-          if (!mbar_wait(b_b1, hh & 1)) ok = false;
-          issue_sh(hh + 1);
-        }
-        if (!mbar_wait(b_mr, hh & 1)) ok = false;  // M tile of head hh written; dM, Yc read back
+      if (cw == 1) {
+        // batch 1 of head hh: dM = dy x^T, dXs = B dS^T (buffer hh&1), Yc = C H^T
+        auto batch1 = [&](int hh) {
+          const int buf = hh & 1;
+          const uint8_t* sX = sXb + buf * kTok;
+          const uint8_t* sY = sYb + buf * kTok;
+          for (int ks = 0; ks < 4; ++ks) mma_bf16(tDM, kdesc_tok(sY, ks), kdesc_tok(sX, ks), id128, ks > 0);
+          for (int ks = 0; ks < p.N / 16; ++ks) {
+            mma_bf16(tDXS + buf * 64, kdesc_c(sB, ks), mndesc_rows(sS, ks), id64, ks > 0);
+            mma_bf16(tYC, kdesc_c(sC, ks), mndesc_rows(sH, ks), id64, ks > 0);
+          }
+          mma_commit(b_b1);
+        };
+        if (!mbar_wait(b_bc, 0)) ok = false;
         tc_fence_after();
-        const uint8_t* sY = sYb + buf * kTok;
-        for (int ks = 0; ks < kRows / 16; ++ks) {  // dX = M^T dy (M = j, N = 64, K = tokens i)
-          const uint64_t da = smem_desc(smem_u32(sA) + ks * 16 * 128, kTok, 1024, kSwz128);
-          mma_bf16(tDX, da, mndesc_rows(sY, ks), id64t, ks > 0);
-        }
-        mma_commit(b_dx);
-        if (hh + 1 < hpg) {  // batch 1 of the next head runs under this head's epilogue; its dXs
-          // buffer was last read by the epilogue of head hh-1
-          if (hh >= 1 && !mbar_wait(b_ed, (hh - 1) & 1)) ok = false;
+        for (int ks = 0; ks < p.N / 16; ++ks)  // C B^T (M = i, N = j, K = d_state), once per group
+          mma_bf16(tCB, kdesc_c(sC, ks), kdesc_c(sB, ks), id128, ks > 0);
+        if (!mbar_wait(&b_xy[0], 0)) ok = false;
+        if (!mbar_wait(b_sh, 0)) ok = false;
+        tc_fence_after();
+        batch1(0);  // its commit also covers C B^T
+        for (int hh = 0; hh + 1 < hpg; ++hh) {
+          const int buf = hh & 1;
+          if (hh >= 1) {  // x, dy of head hh+1 into the buffer head hh-1 used, once its epilogue
+            // has read them (that epilogue waited for the head's MMAs)
+            if (!mbar_wait(b_ed, (hh - 1) & 1)) ok = false;
+            issue_xy(hh + 1);
+          }
+          if (!mbar_wait(b_b1, hh & 1)) ok = false;  // dS, H of head hh+1 once batch 1 of head hh read them
+          issue_sh(hh + 1);
+          // batch 1 of the next head runs under this head's epilogue: dM and Yc of head
+          // hh have been read back; its dXs buffer was last read by the epilogue of head hh-1
+          if (!mbar_wait(b_mr, hh & 1)) ok = false;
           if (!mbar_wait(&b_xy[buf ^ 1], ((hh + 1) >> 1) & 1)) ok = false;
           if (!mbar_wait(b_sh, (hh + 1) & 1)) ok = false;
           tc_fence_after();
           batch1(hh + 1);
+        }
+      } else {
+        for (int hh = 0; hh < hpg; ++hh) {
+          const int buf = hh & 1;
+          if (!mbar_wait(b_mr, hh & 1)) ok = false;  // M tile of head hh written
+          tc_fence_after();
+          const uint8_t* sY = sYb + buf * kTok;
+          for (int ks = 0; ks < kRows / 16; ++ks) {  // dX = M^T dy (M = j, N = 64, K = tokens i)
+            const uint64_t da = smem_desc(smem_u32(sA) + ks * 16 * 128, kTok, 1024, kSwz128);
+            mma_bf16(tDX, da, mndesc_rows(sY, ks), id64t, ks > 0);
+          }
+          mma_commit(b_dx);
         }
       }
     }
@@ -809,7 +816,7 @@ cudaError_t launch_chunk_bwd_group_tc(const Plan& p, const Bufs& f, cudaStream_t
   cudaError_t e = cudaFuncSetAttribute(chunk_bwd_group_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  chunk_bwd_group_tc_kernel<<<dim3(p.nc, p.G, p.b), kThr, smem, s>>>(p, f, X, Y, B, C, S, H);
+  chunk_bwd_group_tc_kernel<<<dim3(p.nc, p.G, p.b), kThrT, smem, s>>>(p, f, X, Y, B, C, S, H);
   return cudaGetLastError();
 }
 

@@ -17,7 +17,7 @@ enum : int { kDevTimeout = 1 };
 // (kSpThreads threads x 4 floats) over a segment of consecutive chunks:
 // kSpSegF in the forward scan, kSpSegB in the reverse scan (which also stages
 // the fp32 carry-in states, so its segments are half as long).
-constexpr int kSpThreads = 256;
+constexpr int kSpThreads = 128;
 constexpr int kSpElems = kSpThreads * 4;
 constexpr int kSpSegF = 16;
 constexpr int kSpSegB = 8;
