@@ -1,0 +1,70 @@
+"""Host-side logic of bench.py (CPU only): the algorithmic byte model, the
+guard on the recorded DRAM traffic, and the reference arm's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_kernel_model_counts_compulsory_bytes():
+    cfg = dict(batch=2, seqlen=300, nheads=4, headdim=16, dstate=8, ngroups=2, chunk=64)
+    m, layer_io = bench.kernel_model(cfg, 2)
+    T, nc = 2 * 300, 5
+    tokx, tokbc = T * 4 * 16 * 2, T * 2 * 8 * 2
+    st32 = 2 * 4 * nc * 16 * 8 * 4
+    per_tok = 2 * 4 * nc * 64 * 4
+    # chunk_scan reads x, B, C, the carry-in states, l and dt, writes y
+    assert m["chunk_scan"]["bytes"] == 2 * tokx + 2 * tokbc + st32 // 2 + 2 * per_tok
+    # forward scan: fp32 chunk states in, carry-in states out in the dtype
+    assert m["state_passing_fwd"]["bytes"] == st32 + st32 // 2
+    # reverse scan: dHloc and the fp32 carry-in states in, dS out
+    assert m["state_passing_bwd"]["bytes"] == 2 * st32 + st32 // 2
+    # the layer's own inputs and outputs, forward plus backward
+    assert layer_io == (2 * tokx + T * 4 * 2 + 2 * tokbc) + (3 * tokx + 2 * T * 4 * 2 + 4 * tokbc)
+
+
+def test_recorded_traffic_only_for_unchanged_sources(monkeypatch):
+    name = "chunk_bwd_tc"
+    files, nbytes, sha = bench.NCU_TRAFFIC[name]
+    # the figure belongs to one workload
+    assert bench.ncu_traffic(name, "tiny_fp32") is None
+    assert bench.ncu_traffic("no_such_kernel", bench.NCU_TRAFFIC_WORKLOAD) is None
+    # a different source hash (the kernel changed since the capture) -> null
+    monkeypatch.setitem(bench.NCU_TRAFFIC, name, (files, nbytes, "0" * 40))
+    assert bench.ncu_traffic(name, bench.NCU_TRAFFIC_WORKLOAD) is None
+
+
+def test_reference_arm_prints_one_contract_line():
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0")
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                          "--warmup", "3", "--workload", "tiny_fp32"], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "tiny_fp32"
+
+
+@pytest.mark.parametrize("rank", ["1"])
+def test_reference_arm_other_ranks_exit_without_work(rank):
+    env = dict(os.environ, WORLD_SIZE="2", RANK=rank)
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                          "--warmup", "3", "--workload", "tiny_fp32"], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0
+    assert not [ln for ln in out.stdout.splitlines() if ln.startswith("{")]

@@ -65,6 +65,10 @@ SMALL = {
                                seq_lengths=[5000, 1, 7806]),
     "fp32_many_segments": dict(batch=1, seqlen=32 * 150, nheads=2, headdim=16, dstate=16,
                                ngroups=1, chunk=32, dtype="f32", init=True, dfinal=True),
+    # chunk 32: tensor-core chunk states next to the CUDA-core scan and backward
+    "bf16_Q32_mixed": dict(batch=1, seqlen=32 * 9 + 11, nheads=4, headdim=64, dstate=64,
+                           ngroups=2, chunk=32, dtype="bf16", init=True, dfinal=True,
+                           seq_lengths=[100, 210]),
 }
 
 
