@@ -68,7 +68,7 @@ SMALL = {
     # chunk 32: tensor-core chunk states next to the CUDA-core scan and backward
     "bf16_Q32_mixed": dict(batch=1, seqlen=32 * 9 + 11, nheads=4, headdim=64, dstate=64,
                            ngroups=2, chunk=32, dtype="bf16", init=True, dfinal=True,
-                           seq_lengths=[100, 210]),
+                           seq_lengths=[100, 199]),
 }
 
 
