@@ -88,14 +88,14 @@ def kernel_model(cfg, dtype_bytes):
 # is the one captured, else null.
 NCU_TRAFFIC_WORKLOAD = "b2_L8192_bf16"
 NCU_TRAFFIC = {
-    "chunk_bwd_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.336e+08, "7db83019a35065adb52ae2d282d9a2dce4b7ee70"),
-    "chunk_bwd_dbc_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.642e+08, "7db83019a35065adb52ae2d282d9a2dce4b7ee70"),
-    "chunk_scan_tc": (('k_chunk_scan_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.554e+08, "8d9f33125ea931225e5c7dbc0046ce0dc4ae72a9"),
-    "chunk_state_tc": (('k_chunk_state_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.853e+08, "df92163105b60f19eb51171ba07e76d9b980c645"),
-    "chunk_dstate_tc": (('k_chunk_state_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.798e+08, "df92163105b60f19eb51171ba07e76d9b980c645"),
-    "state_passing_fwd": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.967e+08, "e329d09e0456a47222a119dfafa261e087eebd75"),
-    "state_passing_fwd_keep": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.333e+08, "e329d09e0456a47222a119dfafa261e087eebd75"),
-    "state_passing_bwd": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.544e+08, "e329d09e0456a47222a119dfafa261e087eebd75"),
+    "chunk_bwd_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.337e+08, "6c4e7c1bf87e51993efe579775ecaa4c493f5b31"),
+    "chunk_bwd_dbc_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.643e+08, "6c4e7c1bf87e51993efe579775ecaa4c493f5b31"),
+    "chunk_scan_tc": (('k_chunk_scan_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.553e+08, "93ea9b99f762e1d29de0b41a8f939b752458acac"),
+    "chunk_state_tc": (('k_chunk_state_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.852e+08, "df92163105b60f19eb51171ba07e76d9b980c645"),
+    "chunk_dstate_tc": (('k_chunk_state_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.797e+08, "df92163105b60f19eb51171ba07e76d9b980c645"),
+    "state_passing_fwd": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.973e+08, "e329d09e0456a47222a119dfafa261e087eebd75"),
+    "state_passing_fwd_keep": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.331e+08, "e329d09e0456a47222a119dfafa261e087eebd75"),
+    "state_passing_bwd": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.541e+08, "e329d09e0456a47222a119dfafa261e087eebd75"),
 }
 
 

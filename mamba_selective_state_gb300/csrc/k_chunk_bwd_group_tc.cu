@@ -455,6 +455,7 @@ __global__ void __launch_bounds__(kThrT, 1) chunk_bwd_group_tc_kernel(Plan p, Bu
         duP[wg * kRows + j] = du;
         dyxP[wg * kRows + j] = tok_ok ? dyx : 0.0f;
         tc_fence_before();
+        fence_async_smem();  // x and dy are next written by tensor copies (async proxy)
         named_sync_compute();  // dX, dXs, x, dy of this head read back; du, dy.x partials complete
         if (tid == 0) mbar_arrive(b_ed);
         if (wg == 0) {

@@ -178,8 +178,10 @@ __global__ void __launch_bounds__(kThr) chunk_bwd_tc_kernel(Plan p, Bufs f,
       if (I * kRows >= len) continue;
       const bool diag = (I == J);
       // every thread has finished its waits on both barriers' previous phases
-      // before thread 0 arms them again
+      // before thread 0 arms them again; its shared reads of the tiles come
+      // before the tensor copies that overwrite them
       tc_fence_before();
+      fence_async_smem();
       __syncthreads();
       if (tid == 0) {
         mbar_expect_tx(&bar[0], 2 * tok_bytes + 2 * c_bytes);
@@ -492,6 +494,7 @@ __global__ void __launch_bounds__(kThr) chunk_bwd_dbc_tc_kernel(Plan p, Bufs f,
       const uint8_t* bJ = sBT;
       const uint8_t* xJ = sXT;
       tc_fence_before();
+      fence_async_smem();  // shared reads of the tiles before the copies that overwrite them
       __syncthreads();  // all threads are past their previous barrier waits
       if (J != TB) {
         if (tid == 0) {
@@ -570,6 +573,7 @@ __global__ void __launch_bounds__(kThr) chunk_bwd_dbc_tc_kernel(Plan p, Bufs f,
       const uint8_t* cI = sCT;
       const uint8_t* yI = sYT;
       tc_fence_before();
+      fence_async_smem();  // shared reads of the tiles before the copies that overwrite them
       __syncthreads();  // all threads are past their previous barrier waits
       if (I != TB) {
         if (tid == 0) {
@@ -643,6 +647,7 @@ __global__ void __launch_bounds__(kThr) chunk_bwd_dbc_tc_kernel(Plan p, Bufs f,
       mma_commit(&bar[1]);
     }
     if (!wait_mma(&bar[1], ph_mma)) ok = false;
+    fence_async_smem();  // shared reads of the tiles before the copies that overwrite them
     __syncthreads();  // before the next head's loads overwrite x/dy/dS/H and lq/dq
   }
   // ---- epilogue: rows of dB and dC for the own block.  tcgen05.ld is a

@@ -296,6 +296,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_scan_tc_kernel(Plan p, Bufs f,
       float a[16], b[16];
       tmem_ld16x2(tmem_addr(tY + buf * 128, wlane, q * 16), tmem_addr(tY + buf * 128 + 64, wlane, q * 16), a, b);
       tc_fence_before();
+      fence_async_smem();  // the x tile is next written by a tensor copy (async proxy)
       __syncwarp();
       if (lane == 0) mbar_arrive(&b_yfree[buf]);  // accumulator pair and x tile released
       const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
