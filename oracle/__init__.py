@@ -11,4 +11,7 @@ and imports nothing from it.
                   and backward, returning the intermediates as well.
   scan         -- the pair-combine operator of the associative scan and a
                   Hillis-Steele log-step scan built on it.
+  gated_norm   -- numpy float64 gated RMSNorm of the Mamba-2 block (the
+                  normalisation after the scan), forward and hand-derived
+                  reverse mode.
 """
