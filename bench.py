@@ -13,6 +13,10 @@ own copy of the workload (independent problems, no collective): weak scaling,
 ``--impl reference`` times the float64 CPU oracle instead (rank 0 only), each
 step a bounded prefix of the same workload.
 
+``--op gated_rmsnorm`` measures the Mamba-2 block's gated RMSNorm instead
+(forward + backward through the C ABI) on the norm that follows the
+workload's scan: rows = tokens, dim = nheads * headdim, group = dim / ngroups.
+
 Prints one JSON line (rank 0).
 """
 from __future__ import annotations
@@ -486,6 +490,173 @@ def run_e2e(inp, dev, args, stream):
                        "the neighbouring steps' compute"}
 
 
+# ----------------------------------------------------------------------------
+# gated RMSNorm of the Mamba-2 block (--op gated_rmsnorm)
+# ----------------------------------------------------------------------------
+NORM_METRIC = "gated RMSNorm fwd+bwd tokens/s (ms); % of HBM"
+
+
+def norm_model(rows, dim, G, gate, s):
+    """Compulsory bytes of each norm kernel: every input read once, every
+    output written once (the backward's per-block dweight partials and their
+    fold are not counted: they are the reduction's own traffic)."""
+    e = rows * dim * s
+    nt = 2 if gate else 1
+    return {"gated_norm_fwd": dict(bytes=nt * e + e + rows * G * 4 + dim * 4, flops=0),
+            "gated_norm_bwd": dict(bytes=(nt + 1) * e + nt * e + 2 * dim * 4, flops=0)}
+
+
+def norm_oracle_seconds(inp, block_rows=1024):
+    """One float64 oracle fwd+bwd over every row of ``inp``, by row blocks."""
+    import torch
+    from oracle import gated_norm
+    w = inp.f64("weight")
+    t0 = time.perf_counter()
+    for r0 in range(0, inp.rows, block_rows):
+        sl = slice(r0, min(inp.rows, r0 + block_rows))
+        y = inp.y[sl].to(torch.float64).numpy()
+        z = None if inp.z is None else inp.z[sl].to(torch.float64).numpy()
+        d = inp.dout[sl].to(torch.float64).numpy()
+        gated_norm.gated_rmsnorm_fwd(y, z, w, inp.group_size, inp.eps)
+        gated_norm.gated_rmsnorm_bwd(y, z, w, d, inp.group_size, inp.eps)
+    return time.perf_counter() - t0
+
+
+def norm_config(name, inp):
+    return {"workload": f"gated_rmsnorm after {name}", "rows": inp.rows, "dim": inp.dim,
+            "group_size": inp.group_size, "eps": inp.eps, "gate": inp.z is not None}
+
+
+def run_norm_reference(args, rank):
+    if rank != 0:
+        return
+    from mamba_selective_state_gb300.inputs import make_norm_workload
+    inp = make_norm_workload(args.workload, seed=0)
+    for _ in range(min(args.warmup, 1)):
+        norm_oracle_seconds(inp)
+    times = [norm_oracle_seconds(inp) for _ in range(max(1, min(args.steps, 5)))]
+    value = inp.rows * len(times) / sum(times)
+    desc = f"float64 numpy oracle fwd+bwd over all {inp.rows} rows, 1024-row blocks, 1 thread"
+    line = {"impl": "reference", "op": "gated_rmsnorm", "metric": NORM_METRIC, "value": value,
+            "unit": "tokens/s", "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": norm_config(args.workload, inp),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_norm(args, world, rank, local):
+    import torch
+    from mamba_selective_state_gb300 import _lib
+    from mamba_selective_state_gb300.inputs import make_norm_workload
+    from mamba_selective_state_gb300.runner import NormDevice
+
+    inp = make_norm_workload(args.workload, seed=rank)
+    dev = NormDevice(inp, device=f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=f"cuda:{local}")
+
+    def step():
+        dev.fwd(stream=stream)
+        dev.bwd(stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    _lib.profile_start()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    prof = _lib.profile_stop()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    tot_ms = max_over_ranks(world, sum(s.elapsed_time(e) for s, e in zip(starts, ends)))
+    ms_per_step = tot_ms / args.steps
+    value = world * inp.rows * args.steps / (tot_ms / 1e3)
+
+    # end to end: inputs from pinned host memory, outputs back, copies and
+    # compute one after the other on the launching stream
+    names_in = ["y", "z", "weight", "dout"] if dev.z is not None else ["y", "weight", "dout"]
+    names_out = ["out", "rstd", "dy", "dweight"] + (["dz"] if dev.dz is not None else [])
+    host_in = {n: getattr(dev, n).to("cpu").pin_memory() for n in names_in}
+    host_out = {n: torch.empty_like(getattr(dev, n), device="cpu").pin_memory() for n in names_out}
+    bi = sum(t.numel() * t.element_size() for t in host_in.values())
+    bo = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for n, t in host_in.items():
+            getattr(dev, n).copy_(t, non_blocking=True)
+        step()
+        for n, t in host_out.items():
+            t.copy_(getattr(dev, n), non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    e2e = {"value": inp.rows / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+           "overlap": "none: copies in, fwd+bwd and copies out in turn on one stream"}
+
+    peaks, src = load_peaks()
+    s_bytes = 2 if inp.dtype == "bf16" else 4
+    model = norm_model(inp.rows, inp.dim, inp.dim // inp.group_size, dev.z is not None, s_bytes)
+    kernels = {k: {"launches": n, "ms_per_launch": ms / n} for k, (n, ms) in prof.items()
+               if not k.startswith("_")}
+    for k, v in kernels.items():
+        if k in model:
+            v["GBps"] = model[k]["bytes"] / (v["ms_per_launch"] / 1e3) / 1e9
+    dom = max(kernels, key=lambda k: kernels[k]["launches"] * kernels[k]["ms_per_launch"])
+    hbm_peak = peaks["hbm_gbs"]
+    ach = kernels[dom].get("GBps", 0.0)
+    roof = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+            "frac": ach / hbm_peak, "traffic": None, "kernel": dom,
+            "peak_source": f"{src} hbm_gbs", "algorithmic_bytes": model.get(dom, {}).get("bytes"),
+            "ms_per_launch": kernels[dom]["ms_per_launch"]}
+    io = model["gated_norm_fwd"]["bytes"] + model["gated_norm_bwd"]["bytes"]
+    line = {"op": "gated_rmsnorm", "metric": NORM_METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": inp.dtype, "data": "synthetic",
+            "config": dict(norm_config(args.workload, inp),
+                           l2="flushed between steps (256 MB write, outside the events)",
+                           parallelism="replicas" if world > 1 else "single GPU"),
+            "roofline": roof,
+            "layer_roofline": {"compulsory_io_bytes": io,
+                               "achieved_GBps": io / (ms_per_step / 1e3) / 1e9,
+                               "frac_of_hbm": io / (ms_per_step / 1e3) / 1e9 / hbm_peak},
+            "e2e": e2e, "gpu_launches": sum(v["launches"] for v in kernels.values()),
+            "kernels": kernels, "clocks": clk}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs = norm_oracle_seconds(inp)
+        line["cpu_baseline"] = {"value": inp.rows / secs, "unit": "tokens/s", "cores": 1,
+                                "kind": "oracle", "seconds": secs,
+                                "sample": f"float64 numpy oracle fwd+bwd over all {inp.rows} "
+                                          "rows, 1024-row blocks, 1 thread"}
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -494,11 +665,16 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="ssd", choices=["ssd", "gated_rmsnorm"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":  # host-only: rank 0 runs, the other ranks exit
-        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+        rank0 = int(os.environ.get("RANK", "0"))
+        if args.op == "gated_rmsnorm":
+            run_norm_reference(args, rank0)
+        else:
+            run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), rank0)
         return
     world, rank, local = dist_setup(args)
     import __graft_entry__
@@ -507,7 +683,7 @@ def main():
     barrier(world)
     if world > 1 and rank != 0:
         __graft_entry__.build()
-    line = run_gpu(args, world, rank, local)
+    line = (run_norm if args.op == "gated_rmsnorm" else run_gpu)(args, world, rank, local)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -155,6 +155,57 @@ int ssd_fwd_noalloc(const ssd_problem* prob, const void* x, const void* dt, cons
                     const float* initial_states, const int32_t* seq_idx, void* y,
                     float* final_states, ssd_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Gated RMSNorm of the Mamba-2 block: the normalisation the block applies to
+ * the scan's output y, gated by the block's z branch.  Page "B200 Helion
+ * Mamba-2" (aitrends.kr/articles/109906) measures its backward
+ * (`_layer_norm_bwd`, a memory-bound row reduction) at batch 2, seqlen 8192,
+ * bf16, without writing out the operation; it is read as
+ *
+ *   g[r,j]    = y[r,j] * silu(z[r,j])        (g = y without SSD_NORM_HAS_Z)
+ *   rstd[r,k] = 1 / sqrt(mean_{j in group k} g[r,j]^2 + eps)
+ *   out[r,j]  = g[r,j] * rstd[r,k] * weight[j]
+ *
+ * over rows r (tokens) and groups k of group_size contiguous columns (in the
+ * Mamba-2 block: dim = nheads * headdim, group_size = dim / ngroups).  The
+ * backward gives dy, dz and dweight = sum over rows of dout * g * rstd; that
+ * sum is folded across thread blocks in a fixed order (page "Cake RMSNorm",
+ * blog.secrett2633.cloud, flashinfer PR 6997, section "Fixed-order tree fold
+ * reduction"), so dweight is bitwise reproducible run to run on one device.
+ *
+ * Layouts (dense row-major, device memory, 16-byte aligned):
+ *   y, z, out, dout, dy, dz   (rows, dim)   dtype
+ *   weight, dweight           (dim)         fp32
+ *   rstd                      (rows, dim / group_size) fp32
+ * Limits: dim % group_size == 0; group_size a multiple of 8 (bf16) or 4
+ * (fp32) and at most 4096 (bf16) or 2048 (fp32); eps >= 0.
+ * Ownership, errors and stream semantics as above.  The calls have no
+ * device-side waits and use no status word. */
+enum { SSD_NORM_HAS_Z = 1 /* z (the gate) is given */ };
+
+typedef struct {
+  int64_t rows, dim, group_size;
+  float eps;
+  int32_t dtype; /* ssd_dtype of y, z, out, dout, dy, dz */
+  int32_t flags; /* SSD_NORM_HAS_Z */
+} ssd_norm_problem;
+
+/* Forward: writes out and, if non-NULL, rstd.  z must be non-NULL iff
+ * SSD_NORM_HAS_Z. */
+int ssd_gated_rmsnorm_fwd(const ssd_norm_problem* prob, const void* y, const void* z,
+                          const float* weight, void* out, float* rstd, ssd_stream_t stream);
+
+/* Bytes of device workspace ssd_gated_rmsnorm_bwd needs (the per-block
+ * dweight partials; a pure function of the problem, 0 if it is invalid). */
+size_t ssd_gated_rmsnorm_bwd_workspace_bytes(const ssd_norm_problem* prob);
+
+/* Backward for the upstream gradient dout (rstd is recomputed from y and z).
+ * Overwrites dy, dz (non-NULL iff SSD_NORM_HAS_Z) and dweight. */
+int ssd_gated_rmsnorm_bwd(const ssd_norm_problem* prob, const void* y, const void* z,
+                          const float* weight, const void* dout, void* dy, void* dz,
+                          float* dweight, void* workspace, size_t workspace_bytes,
+                          ssd_stream_t stream);
+
 /* Library build/version string, e.g. "libssd 0.1 sm_103a". */
 const char* ssd_version(void);
 

@@ -26,11 +26,14 @@ SSD_HAS_SEQ_IDX = 2
 SSD_HAS_DFINAL = 4
 SSD_WANT_DINIT = 8
 SSD_TEST_DROP_SCAN_PUBLISH = 1 << 16
+SSD_NORM_HAS_Z = 1
 
 # every symbol include/ssd.h declares
 EXPORTS = ["ssd_fwd_workspace_bytes", "ssd_bwd_workspace_bytes", "ssd_fwd", "ssd_bwd",
            "ssd_status_string", "ssd_read_device_status", "ssd_version", "ssd_profile_start",
-           "ssd_profile_stop", "ssd_profile_count", "ssd_profile_get", "ssd_fwd_noalloc"]
+           "ssd_profile_stop", "ssd_profile_count", "ssd_profile_get", "ssd_fwd_noalloc",
+           "ssd_gated_rmsnorm_fwd", "ssd_gated_rmsnorm_bwd_workspace_bytes",
+           "ssd_gated_rmsnorm_bwd"]
 SSD_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -40,6 +43,12 @@ class ssd_problem(ctypes.Structure):
                 ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
                 ("chunk_size", ctypes.c_int64), ("dtype", ctypes.c_int32),
                 ("flags", ctypes.c_int32)]
+
+
+class ssd_norm_problem(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("dim", ctypes.c_int64),
+                ("group_size", ctypes.c_int64), ("eps", ctypes.c_float),
+                ("dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class SSDError(RuntimeError):
@@ -76,6 +85,13 @@ def _load():
     lib.ssd_profile_get.restype = i32
     lib.ssd_fwd_noalloc.argtypes = [pp] + [vp] * 11 + [vp]
     lib.ssd_fwd_noalloc.restype = i32
+    npp = ctypes.POINTER(ssd_norm_problem)
+    lib.ssd_gated_rmsnorm_fwd.argtypes = [npp] + [vp] * 5 + [vp]
+    lib.ssd_gated_rmsnorm_fwd.restype = i32
+    lib.ssd_gated_rmsnorm_bwd_workspace_bytes.argtypes = [npp]
+    lib.ssd_gated_rmsnorm_bwd_workspace_bytes.restype = sz
+    lib.ssd_gated_rmsnorm_bwd.argtypes = [npp] + [vp] * 8 + [sz, vp]
+    lib.ssd_gated_rmsnorm_bwd.restype = i32
     return lib
 
 
@@ -182,3 +198,36 @@ def ssd_fwd_noalloc(prob, x, dt, dt_bias, A, B, C, D, initial_states, seq_idx, y
     return int(LIB.ssd_fwd_noalloc(ctypes.byref(prob), _p(x), _p(dt), _p(dt_bias), _p(A), _p(B),
                                    _p(C), _p(D), _p(initial_states), _p(seq_idx), _p(y),
                                    _p(final_states), _stream(stream)))
+
+
+def make_norm_problem(rows, dim, group_size, eps, dtype, gate=True) -> ssd_norm_problem:
+    if isinstance(dtype, torch.dtype):
+        dtype = SSD_BF16 if dtype == torch.bfloat16 else SSD_F32
+    return ssd_norm_problem(rows, dim, group_size, eps, dtype, SSD_NORM_HAS_Z if gate else 0)
+
+
+def ssd_gated_rmsnorm_bwd_workspace_bytes(prob: ssd_norm_problem) -> int:
+    return int(LIB.ssd_gated_rmsnorm_bwd_workspace_bytes(ctypes.byref(prob)))
+
+
+def ssd_gated_rmsnorm_fwd(prob, y, z, weight, out, rstd=None, stream=None, check=True) -> int:
+    """Enqueue the gated RMSNorm forward on ``stream`` (default: torch's
+    current stream)."""
+    rc = LIB.ssd_gated_rmsnorm_fwd(ctypes.byref(prob), _p(y), _p(z), _p(weight), _p(out),
+                                   _p(rstd), _stream(stream))
+    if check and rc != SSD_OK:
+        raise SSDError(rc, "ssd_gated_rmsnorm_fwd")
+    return rc
+
+
+def ssd_gated_rmsnorm_bwd(prob, y, z, weight, dout, dy, dz, dweight, workspace,
+                          workspace_bytes=None, stream=None, check=True) -> int:
+    """Enqueue the gated RMSNorm backward on ``stream``."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = LIB.ssd_gated_rmsnorm_bwd(ctypes.byref(prob), _p(y), _p(z), _p(weight), _p(dout),
+                                   _p(dy), _p(dz), _p(dweight), _p(workspace), workspace_bytes,
+                                   _stream(stream))
+    if check and rc != SSD_OK:
+        raise SSDError(rc, "ssd_gated_rmsnorm_bwd")
+    return rc

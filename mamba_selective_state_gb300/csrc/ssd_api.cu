@@ -164,6 +164,8 @@ int device_sm_count() {
   return current_device_info(&d) ? d.sms : 148;
 }
 
+int device_check() { return check_device(); }
+
 }  // namespace ssd
 
 using namespace ssd;

@@ -174,3 +174,72 @@ def make_workload(name: str, seed: int = 0, **overrides) -> SSDInputs:
         cfg["seqlen"] = sum(lens)
         cfg["seq_lengths"] = lens
     return make_inputs(rng=rng, **cfg)
+
+
+# ---------------------------------------------------------------------------
+# Gated RMSNorm of the Mamba-2 block (the normalisation after the scan).
+#
+# Recipe (numpy PCG64 ``default_rng(seed)``, draw order y, z, weight, dout):
+#   y, z, dout ~ N(0, 1)   (y has the scan output's unit scale, z the gate's)
+#   weight = 1 + 0.1 * N(0, 1)   (the usual all-ones start, perturbed so that
+#                                 a dropped or misplaced weight shows)
+#   eps = 1e-5
+# Shapes follow the layer workloads: rows = tokens (batch * seqlen, or the
+# packed total), dim = nheads * headdim, group_size = dim / ngroups.
+
+@dataclasses.dataclass
+class NormInputs:
+    """One gated-RMSNorm problem's inputs as CPU torch tensors."""
+    rows: int
+    dim: int
+    group_size: int
+    eps: float
+    dtype: str                      # "bf16" or "f32"
+    y: torch.Tensor                 # (rows, dim)
+    z: Optional[torch.Tensor]       # (rows, dim), None without a gate
+    weight: torch.Tensor            # (dim,) fp32
+    dout: torch.Tensor              # (rows, dim)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    def f64(self, name: str) -> Optional[np.ndarray]:
+        t = getattr(self, name)
+        return None if t is None else t.to(torch.float64).numpy().copy()
+
+
+def make_norm_inputs(rows, dim, group_size, dtype="bf16", gate=True, eps=1e-5, seed=0,
+                     rng=None) -> NormInputs:
+    if dim % group_size != 0:
+        raise ValueError("group_size must divide dim")
+    if rng is None:
+        rng = np.random.default_rng(seed)
+    f32 = np.float32
+    y = rng.standard_normal((rows, dim), dtype=f32)
+    z = rng.standard_normal((rows, dim), dtype=f32)
+    w = 1.0 + 0.1 * rng.standard_normal(dim)
+    dout = rng.standard_normal((rows, dim), dtype=f32)
+    return NormInputs(rows=rows, dim=dim, group_size=group_size, eps=eps, dtype=dtype,
+                      y=_round(y, dtype), z=_round(z, dtype) if gate else None,
+                      weight=torch.from_numpy(w.astype(f32)), dout=_round(dout, dtype))
+
+
+def norm_shape(name: str, seed: int = 0) -> dict:
+    """(rows, dim, group_size, dtype) of the gated norm that follows the scan
+    of layer workload ``name``."""
+    cfg = WORKLOADS[name]
+    if "nseq" in cfg:
+        rng = np.random.default_rng(seed)
+        rows = sum(draw_lengths(rng, cfg["nseq"], cfg["min_len"], cfg["max_len"],
+                                cfg["max_total"]))
+    else:
+        rows = cfg["batch"] * cfg["seqlen"]
+    dim = cfg["nheads"] * cfg["headdim"]
+    return dict(rows=rows, dim=dim, group_size=dim // cfg["ngroups"], dtype=cfg["dtype"])
+
+
+def make_norm_workload(name: str, seed: int = 0, gate=True, **overrides) -> NormInputs:
+    shape = norm_shape(name, seed)
+    shape.update(overrides)
+    return make_norm_inputs(gate=gate, seed=seed, **shape)

@@ -6,7 +6,7 @@ from __future__ import annotations
 import torch
 
 from . import _lib
-from .inputs import SSDInputs
+from .inputs import NormInputs, SSDInputs
 
 
 class SSDDevice:
@@ -84,4 +84,42 @@ class SSDDevice:
                        dA=self.dA, dD=self.dD)
             if self.dinit is not None:
                 out["dinitial_states"] = self.dinit
+        return {k: v.detach().to("cpu", torch.float64) for k, v in out.items()}
+
+
+class NormDevice:
+    """Device buffers of one gated-RMSNorm problem (inputs, out, rstd, the
+    gradients and the backward workspace) and its calls through the C ABI."""
+
+    def __init__(self, inp: NormInputs, device="cuda"):
+        self.inp = inp
+        dev = torch.device(device)
+        to = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
+        self.y, self.z, self.weight, self.dout = to(inp.y), to(inp.z), to(inp.weight), to(inp.dout)
+        self.prob = _lib.make_norm_problem(inp.rows, inp.dim, inp.group_size, inp.eps,
+                                           inp.torch_dtype, gate=inp.z is not None)
+        self.out = torch.empty_like(self.y)
+        self.rstd = torch.empty((inp.rows, inp.dim // inp.group_size), dtype=torch.float32,
+                                device=dev)
+        self.dy = torch.empty_like(self.y)
+        self.dz = None if self.z is None else torch.empty_like(self.z)
+        self.dweight = torch.empty(inp.dim, dtype=torch.float32, device=dev)
+        ws = _lib.ssd_gated_rmsnorm_bwd_workspace_bytes(self.prob)
+        if ws == 0:
+            raise _lib.SSDError(_lib.SSD_ERR_INVALID_ARGUMENT, "norm workspace size")
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+
+    def fwd(self, stream=None, check=True):
+        return _lib.ssd_gated_rmsnorm_fwd(self.prob, self.y, self.z, self.weight, self.out,
+                                          self.rstd, stream=stream, check=check)
+
+    def bwd(self, stream=None, check=True):
+        return _lib.ssd_gated_rmsnorm_bwd(self.prob, self.y, self.z, self.weight, self.dout,
+                                          self.dy, self.dz, self.dweight, self.workspace,
+                                          stream=stream, check=check)
+
+    def results(self) -> dict:
+        out = dict(out=self.out, rstd=self.rstd, dy=self.dy, dweight=self.dweight)
+        if self.dz is not None:
+            out["dz"] = self.dz
         return {k: v.detach().to("cpu", torch.float64) for k, v in out.items()}

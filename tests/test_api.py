@@ -127,3 +127,57 @@ def test_profile_queries_without_records(lib):
     ms = ctypes.c_double()
     rc = lib.LIB.ssd_profile_get(0, ctypes.byref(name), ctypes.byref(n), ctypes.byref(ms))
     assert rc == lib.SSD_ERR_INVALID_ARGUMENT
+
+
+def nprob(lib, **kw):
+    d = dict(rows=300, dim=4096, group_size=512, eps=1e-5, dtype=lib.SSD_BF16, gate=True)
+    d.update(kw)
+    return lib.make_norm_problem(**d)
+
+
+def test_norm_workspace_sizes(lib):
+    # one fp32 row of dweight partials per row slice: min(rows, 1024) slices
+    assert lib.ssd_gated_rmsnorm_bwd_workspace_bytes(nprob(lib)) == 300 * 4096 * 4
+    assert lib.ssd_gated_rmsnorm_bwd_workspace_bytes(nprob(lib, rows=5000)) == 1024 * 4096 * 4
+    assert lib.ssd_gated_rmsnorm_bwd_workspace_bytes(nprob(lib, rows=1, dim=8, group_size=8)) == 32
+
+
+@pytest.mark.parametrize("bad", [
+    dict(rows=0), dict(dim=0), dict(group_size=0), dict(group_size=500),       # 500 does not divide 4096
+    dict(group_size=4, dtype=1), dict(dim=8192, group_size=8192),             # > 4096 bf16 values
+    dict(dtype=0, dim=4096, group_size=4096), dict(dtype=5), dict(eps=-1.0),
+    dict(eps=float("nan")),
+])
+def test_invalid_norm_problems_have_no_workspace(lib, bad):
+    assert lib.ssd_gated_rmsnorm_bwd_workspace_bytes(nprob(lib, **bad)) == 0
+
+
+def test_norm_limits_are_accepted(lib):
+    # the largest groups of each dtype and the smallest piece
+    for kw in (dict(dim=8192, group_size=4096), dict(dtype=0, dim=4096, group_size=2048),
+               dict(dtype=0, dim=12, group_size=4), dict(dim=24, group_size=8)):
+        assert lib.ssd_gated_rmsnorm_bwd_workspace_bytes(nprob(lib, **kw)) > 0, kw
+
+
+def test_norm_argument_errors(lib):
+    p = nprob(lib)
+    fwd = lambda q, **o: lib.ssd_gated_rmsnorm_fwd(  # noqa: E731
+        q, o.get("y", FAKE), o.get("z", FAKE), o.get("w", FAKE), o.get("out", FAKE),
+        o.get("rstd", None), stream=0, check=False)
+    assert lib.LIB.ssd_gated_rmsnorm_fwd(None, *([None] * 5), None) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert fwd(p, y=None) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert fwd(p, out=None) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert fwd(p, z=None) == lib.SSD_ERR_INVALID_ARGUMENT                  # gate flag, no z
+    assert fwd(nprob(lib, gate=False)) == lib.SSD_ERR_INVALID_ARGUMENT     # z without the flag
+    assert fwd(p, rstd=FAKE + 8) == lib.SSD_ERR_INVALID_ARGUMENT           # misaligned
+    assert fwd(nprob(lib, group_size=500)) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert fwd(nprob(lib, group_size=4)) == lib.SSD_ERR_UNSUPPORTED        # < one bf16 piece
+    bwd = lambda q, ws=1 << 40, **o: lib.ssd_gated_rmsnorm_bwd(  # noqa: E731
+        q, o.get("y", FAKE), o.get("z", FAKE), o.get("w", FAKE), o.get("dout", FAKE),
+        o.get("dy", FAKE), o.get("dz", FAKE), o.get("dw", FAKE), o.get("ws", FAKE),
+        workspace_bytes=ws, stream=0, check=False)
+    assert bwd(p, dout=None) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert bwd(p, dz=None) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert bwd(nprob(lib, gate=False), z=None) == lib.SSD_ERR_INVALID_ARGUMENT   # dz given
+    assert bwd(p, dw=FAKE + 4) == lib.SSD_ERR_INVALID_ARGUMENT
+    assert bwd(p, ws=1024) == lib.SSD_ERR_WORKSPACE_TOO_SMALL

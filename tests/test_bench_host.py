@@ -68,3 +68,29 @@ def test_reference_arm_other_ranks_exit_without_work(rank):
                          capture_output=True, text=True, timeout=300)
     assert out.returncode == 0
     assert not [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_norm_model_counts_compulsory_bytes():
+    rows, dim, G = 100, 64, 4
+    m = bench.norm_model(rows, dim, G, True, 2)
+    e = rows * dim * 2
+    # forward: y, z in; out, rstd out; weight once
+    assert m["gated_norm_fwd"]["bytes"] == 3 * e + rows * G * 4 + dim * 4
+    # backward: y, z, dout in; dy, dz out; weight in, dweight out
+    assert m["gated_norm_bwd"]["bytes"] == 5 * e + 2 * dim * 4
+    m1 = bench.norm_model(rows, dim, G, False, 4)
+    assert m1["gated_norm_bwd"]["bytes"] == 3 * rows * dim * 4 + 2 * dim * 4
+
+
+def test_norm_reference_arm_prints_one_contract_line():
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0")
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--op",
+                          "gated_rmsnorm", "--steps", "1", "--warmup", "3", "--workload",
+                          "tiny_fp32"], cwd=ROOT, env=env, capture_output=True, text=True,
+                         timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["op"] == "gated_rmsnorm" and d["value"] > 0
+    assert d["config"]["rows"] == 256 and d["config"]["group_size"] == 64
