@@ -100,6 +100,10 @@ NCU_TRAFFIC = {
     "state_passing_fwd": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.973e+08, "e329d09e0456a47222a119dfafa261e087eebd75"),
     "state_passing_fwd_keep": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.331e+08, "e329d09e0456a47222a119dfafa261e087eebd75"),
     "state_passing_bwd": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.541e+08, "e329d09e0456a47222a119dfafa261e087eebd75"),
+    # the gated RMSNorm after the same workload's scan (bench.py --op gated_rmsnorm)
+    "gated_norm_fwd": (('k_gated_norm.cu', 'ssd_internal.cuh'), 3.657e+08, "f587d4f32953c50ce64efc0fc949b0aebeecf91f"),
+    "gated_norm_bwd": (('k_gated_norm.cu', 'ssd_internal.cuh'), 6.303e+08, "f587d4f32953c50ce64efc0fc949b0aebeecf91f"),
+    "gated_norm_dw_fold": (('k_gated_norm.cu', 'ssd_internal.cuh'), 3.743e+06, "f587d4f32953c50ce64efc0fc949b0aebeecf91f"),
 }
 
 
@@ -631,7 +635,7 @@ def run_norm(args, world, rank, local):
     hbm_peak = peaks["hbm_gbs"]
     ach = kernels[dom].get("GBps", 0.0)
     roof = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-            "frac": ach / hbm_peak, "traffic": None, "kernel": dom,
+            "frac": ach / hbm_peak, "traffic": ncu_traffic(dom, args.workload), "kernel": dom,
             "peak_source": f"{src} hbm_gbs", "algorithmic_bytes": model.get(dom, {}).get("bytes"),
             "ms_per_launch": kernels[dom]["ms_per_launch"]}
     io = model["gated_norm_fwd"]["bytes"] + model["gated_norm_bwd"]["bytes"]

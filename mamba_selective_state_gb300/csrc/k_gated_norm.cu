@@ -33,6 +33,9 @@
 
 namespace ssd {
 
+// ssd_api.cu: SSD_OK on an sm_103 device, else SSD_ERR_UNSUPPORTED (or SSD_ERR_CUDA).
+int device_check();
+
 namespace {
 
 constexpr int kMaxTeamWarps = 16;   // pieces per group <= 512

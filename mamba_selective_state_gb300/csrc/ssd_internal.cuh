@@ -142,8 +142,6 @@ cudaError_t launch_dt_bwd(const Plan& p, const Bufs& f, cudaStream_t s);
 cudaError_t launch_param_reduce(const Plan& p, const Bufs& f, cudaStream_t s);
 
 int device_sm_count();
-// SSD_OK on an sm_103 device, else SSD_ERR_UNSUPPORTED (or SSD_ERR_CUDA).
-int device_check();
 
 // Tensor-core variants (bf16, headdim 64); the launchers above use them when
 // the problem is inside their supported set.
