@@ -14,4 +14,7 @@ and imports nothing from it.
   gated_norm   -- numpy float64 gated RMSNorm of the Mamba-2 block (the
                   normalisation after the scan), forward and hand-derived
                   reverse mode.
+  context_parallel -- the layer over a sequence split into shards, joined by
+                  exclusive folds of per-shard (decay, state) pairs and of
+                  dinitial states (context parallelism).
 """
