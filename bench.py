@@ -266,10 +266,12 @@ class OracleSample:
                 f"every row ({self.full.batch} rows, all {self.full.nheads} heads) of {self.name}")
 
 
-def cpu_baseline(name, target_s=15.0, min_s=10.0):
+def cpu_baseline(name, target_s=15.0, min_s=10.0, single_core_s=4.0):
     """The oracle on a bounded sample of the workload: a prefix sized to about
     target_s seconds, repeated (whole workload too small) until at least
-    min_s seconds of CPU work have been timed."""
+    min_s seconds of CPU work have been timed, on every host core; then a
+    shorter prefix on one core (``single_core``)."""
+    from oracle import ssd_ref
     smp = OracleSample(name, target_s)
     secs, threads, reps = 0.0, 1, 0
     while reps == 0 or (secs < min_s and reps < 20):
@@ -278,8 +280,20 @@ def cpu_baseline(name, target_s=15.0, min_s=10.0):
         reps += 1
     tok = smp.full.batch * smp.Lp * reps
     sample = smp.describe() + (f", run {reps} times" if reps > 1 else "")
-    return {"value": tok / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": sample, "seconds": secs}
+    out = {"value": tok / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+           "sample": sample, "seconds": secs}
+    # one core: a prefix sized from the all-core rate to about single_core_s
+    per_tok_1 = secs / tok * threads
+    lp1 = int(max(1, min(smp.full.seqlen, single_core_s / max(per_tok_1 * smp.full.batch, 1e-9))))
+    ssd_ref.set_threads(1)
+    try:
+        t1, th1 = smp.run(lp1)
+    finally:
+        ssd_ref.set_threads(0)
+    out["single_core"] = {"value": smp.full.batch * lp1 / t1, "unit": "tokens/s", "cores": th1,
+                          "seconds": t1,
+                          "sample": f"the first {lp1} tokens of every row, same workload"}
+    return out
 
 
 def run_reference(args, world, rank):

@@ -94,3 +94,10 @@ def test_norm_reference_arm_prints_one_contract_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["op"] == "gated_rmsnorm" and d["value"] > 0
     assert d["config"]["rows"] == 256 and d["config"]["group_size"] == 64
+
+
+def test_cpu_baseline_reports_all_cores_and_one_core():
+    d = bench.cpu_baseline("tiny_fp32", target_s=0.3, min_s=0.2, single_core_s=0.1)
+    assert d["kind"] == "oracle" and d["value"] > 0 and d["cores"] >= 1
+    one = d["single_core"]
+    assert one["cores"] == 1 and one["value"] > 0 and "tokens" in one["sample"]
