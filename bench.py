@@ -126,6 +126,22 @@ def base_name(kname):
     return kname
 
 
+def layer_summary(kernels, model, steps, ms_per_step, layer_io, hbm_peak, tc_peak):
+    """The whole layer against both roofs: its compulsory IO bytes per step
+    over the step time against HBM, and the matrix-product flops of all its
+    launches in a step (the kernel model's flops times launches per step)
+    against the dense bf16 tensor peak."""
+    flops = sum(model[base_name(k)]["flops"] * v["launches"] / steps
+                for k, v in kernels.items() if base_name(k) in model)
+    sec = ms_per_step / 1e3
+    return {"compulsory_io_bytes": layer_io,
+            "achieved_GBps": layer_io / sec / 1e9,
+            "frac_of_hbm": layer_io / sec / 1e9 / hbm_peak,
+            "flops_per_step": flops,
+            "achieved_TFLOPps": flops / sec / 1e12,
+            "frac_of_tensor": flops / sec / 1e12 / tc_peak}
+
+
 def load_peaks():
     try:
         with open(PEAKS_PATH) as fh:
@@ -343,8 +359,10 @@ def run_gpu(args, world, rank, local):
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev.device)
 
-    def step():
+    def step(mid=None):
         dev.fwd(stream=stream)
+        if mid is not None:
+            mid.record(stream)
         dev.bwd(stream=stream)
 
     for _ in range(args.warmup):
@@ -354,6 +372,7 @@ def run_gpu(args, world, rank, local):
         raise RuntimeError("device status word reports an error after warm-up")
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(local) if rank == 0 else None
     barrier(world)
@@ -366,7 +385,7 @@ def run_gpu(args, world, rank, local):
     for i in range(args.steps):
         flush.fill_(float(i))
         starts[i].record(stream)
-        step()
+        step(mids[i])
         ends[i].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
@@ -374,6 +393,7 @@ def run_gpu(args, world, rank, local):
     barrier(world)
     clk = clocks.stop() if clocks else None
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    fwd_ms = [s.elapsed_time(m) for s, m in zip(starts, mids)]
     tot_ms = sum(step_ms)
     tot_ms_max = max_over_ranks(world, tot_ms)
     if dev.device_status(stream) != 0:
@@ -425,9 +445,10 @@ def run_gpu(args, world, rank, local):
             v["GBps"] = mk["bytes"] / d / 1e9
             v["TFLOPps"] = mk["flops"] / d / 1e12
     ms_per_step = tot_ms_max / args.steps
-    layer = {"compulsory_io_bytes": layer_io,
-             "achieved_GBps": layer_io / (ms_per_step / 1e3) / 1e9,
-             "frac_of_hbm": layer_io / (ms_per_step / 1e3) / 1e9 / hbm_peak}
+    layer = layer_summary(kernels, model, args.steps, ms_per_step, layer_io, hbm_peak, tc_peak)
+    layer.update(fwd_ms_mean=statistics.mean(fwd_ms),
+                 bwd_ms_mean=statistics.mean(t - f for t, f in zip(step_ms, fwd_ms)),
+                 step_ms_median=statistics.median(step_ms))
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

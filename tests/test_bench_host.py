@@ -101,3 +101,15 @@ def test_cpu_baseline_reports_all_cores_and_one_core():
     assert d["kind"] == "oracle" and d["value"] > 0 and d["cores"] >= 1
     one = d["single_core"]
     assert one["cores"] == 1 and one["value"] > 0 and "tokens" in one["sample"]
+
+
+def test_layer_summary_against_both_roofs():
+    model = {"chunk_state": dict(bytes=10, flops=1000), "dt_cumsum": dict(bytes=5, flops=0)}
+    kernels = {"chunk_state_tc": {"launches": 4}, "dt_cumsum": {"launches": 4},
+               "unknown": {"launches": 2}}
+    d = bench.layer_summary(kernels, model, steps=2, ms_per_step=1.0, layer_io=2e9,
+                            hbm_peak=4000.0, tc_peak=0.5)
+    assert d["flops_per_step"] == 2000            # two chunk_state launches per step
+    assert abs(d["achieved_GBps"] - 2000.0) < 1e-9 and abs(d["frac_of_hbm"] - 0.5) < 1e-12
+    assert abs(d["achieved_TFLOPps"] - 2e-6) < 1e-18
+    assert abs(d["frac_of_tensor"] - 4e-6) < 1e-18
