@@ -36,3 +36,19 @@ def test_norm_parity_cases_pass_validation():
         out, rstd = gated_norm.gated_rmsnorm_fwd(inp.f64("y"), inp.f64("z"), inp.f64("weight"),
                                                  gs, inp.eps)
         assert out.shape == (rows, dim) and rstd.shape == (rows, dim // gs)
+
+
+def test_norm_shapes_follow_the_layer_workloads():
+    """The norm after each layer workload has one row per token, H*P columns
+    and H*P/G columns per group (the packed workload's rows are its drawn
+    total)."""
+    from mamba_selective_state_gb300.inputs import WORKLOADS, make_workload, norm_shape
+    for name, cfg in WORKLOADS.items():
+        s = norm_shape(name)
+        dim = cfg["nheads"] * cfg["headdim"]
+        assert s["dim"] == dim and s["group_size"] * cfg["ngroups"] == dim
+        if "nseq" in cfg:
+            inp = make_workload(name, seed=0)
+            assert s["rows"] == inp.batch * inp.seqlen
+        else:
+            assert s["rows"] == cfg["batch"] * cfg["seqlen"]
