@@ -181,3 +181,30 @@ def test_norm_argument_errors(lib):
     assert bwd(nprob(lib, gate=False), z=None) == lib.SSD_ERR_INVALID_ARGUMENT   # dz given
     assert bwd(p, dw=FAKE + 4) == lib.SSD_ERR_INVALID_ARGUMENT
     assert bwd(p, ws=1024) == lib.SSD_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_workspace_queries_over_random_shapes(lib):
+    """Over 300 seeded random problems: valid ones get a 256-byte-multiple
+    workspace that grows with the sequence and is larger for the backward;
+    the norm's workspace is one fp32 row per row slice; invalid ones get 0."""
+    import numpy as np
+    rng = np.random.default_rng(11)
+    pow2 = [16, 32, 64, 128]
+    for _ in range(300):
+        P, N = int(rng.choice(pow2)), int(rng.choice(pow2))
+        G = int(rng.integers(1, 5))
+        H = G * int(rng.integers(1, 5))
+        Q = 16 * int(rng.integers(1, 17))
+        b, L = int(rng.integers(1, 4)), int(rng.integers(1, 3000))
+        dt = int(rng.integers(0, 2))
+        p = lib.make_problem(b, L, H, P, N, G, Q, dt)
+        fw, bw = lib.ssd_fwd_workspace_bytes(p), lib.ssd_bwd_workspace_bytes(p)
+        if P * N > 8192:
+            assert fw == 0 and bw == 0
+            continue
+        assert fw > 0 and bw > fw and fw % 256 == 0 and bw % 256 == 0, (b, L, H, P, N, G, Q)
+        longer = lib.make_problem(b, L + Q, H, P, N, G, Q, dt)
+        assert lib.ssd_fwd_workspace_bytes(longer) > fw
+        rows, gs = int(rng.integers(1, 5000)), 8 * int(rng.integers(1, 65))
+        npb = lib.make_norm_problem(rows, gs * G, gs, 1e-5, lib.SSD_BF16, gate=bool(dt))
+        assert lib.ssd_gated_rmsnorm_bwd_workspace_bytes(npb) == min(rows, 1024) * gs * G * 4
