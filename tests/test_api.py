@@ -208,3 +208,17 @@ def test_workspace_queries_over_random_shapes(lib):
         rows, gs = int(rng.integers(1, 5000)), 8 * int(rng.integers(1, 65))
         npb = lib.make_norm_problem(rows, gs * G, gs, 1e-5, lib.SSD_BF16, gate=bool(dt))
         assert lib.ssd_gated_rmsnorm_bwd_workspace_bytes(npb) == min(rows, 1024) * gs * G * 4
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """No fallback: the binding refuses to import when libssd.so is absent."""
+    import shutil
+    import sys
+    pkg = tmp_path / "bindingcopy"
+    pkg.mkdir()
+    (pkg / "__init__.py").write_text("")
+    shutil.copy(os.path.join(ROOT, "mamba_selective_state_gb300", "_lib.py"), pkg / "_lib.py")
+    r = subprocess.run([sys.executable, "-c", "import bindingcopy._lib"], cwd=str(tmp_path),
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libssd.so not built" in r.stderr
