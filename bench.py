@@ -65,17 +65,49 @@ def kernel_model(cfg, dtype_bytes):
     m["state_passing_fwd"] = dict(bytes=st32 + stS, flops=2 * units * P * N)
     # the backward's forward pass also keeps the fp32 carry-in states (in place)
     m["state_passing_fwd_keep"] = dict(bytes=2 * st32 + stS, flops=2 * units * P * N)
+    # chunk_scan: per (group, chunk) C B^T over the row/column tile pairs on
+    # or below the diagonal (at chunk 128 also C_rev B^T, the copy with its
+    # row blocks reversed that balances the mask pass); per head
+    # Y1 = A_hat X over the same tile pairs and Y2 = C H_in^T
+    if Q <= 128:
+        scan_cb = (4 if Q == 128 else 2) * Q * Q * N
+        scan_head = 2 * Q * Q * P + 2 * Q * N * P
+    else:
+        R = 128
+        nb = -(-Q // R)
+        pairs = nb * (nb + 1) // 2
+        scan_cb = pairs * 2 * R * R * N
+        scan_head = pairs * 2 * R * R * P + 2 * Q * N * P
     m["chunk_scan"] = dict(bytes=2 * tokx + 2 * tokbc + stS + 2 * per_tok,
-                           flops=gunits * 2 * Q * Q * N + units * (2 * Q * Q * P + 2 * Q * N * P))
+                           flops=gunits * scan_cb + units * scan_head)
     m["chunk_dstate"] = dict(bytes=tokx + tokbc + per_tok + st32, flops=2 * units * Q * P * N)
     # reads dHloc and the fp32 carry-in states (for dL/da_c), writes dS
     m["state_passing_bwd"] = dict(bytes=2 * st32 + stS, flops=4 * units * P * N)
+    # Backward flops are counted from the matrix products each kernel issues
+    # (2 flops per multiply-add, dense tiles).  Chunks of up to 128 tokens
+    # (one token tile per chunk): the token kernel forms C B^T once per
+    # group and, per head, dM = dy x^T, dX_s = B dS^T, Y_c = C H_in^T and
+    # dX = M^T dY; the dB/dC kernel, per head, dM again, dC += dy H,
+    # dB += x dS, dC += dCB B and dB += dCB^T C.  Chunks of 256 tokens (two
+    # 128-token tiles, R = 128): per head and per tile pair (I >= J, three
+    # pairs) the token kernel forms C B^T and B C^T, dy x^T and x dy^T and
+    # dX += A_hat dY, plus Y_c and dX_s per diagonal tile; the dB/dC kernel
+    # forms dM and one dCB product per (tile, partner) for dC and for dB
+    # (three pairs each), plus the carry and state products per tile.
+    if Q <= 128:
+        bwd_tok_flops = gunits * 2 * Q * Q * N + units * (4 * Q * Q * P + 4 * Q * P * N)
+        bwd_dbc_flops = units * (2 * Q * Q * P + 4 * Q * N * P + 4 * Q * Q * N)
+    else:
+        R = 128
+        nb = -(-Q // R)
+        pairs = nb * (nb + 1) // 2
+        bwd_tok_flops = units * (pairs * (4 * R * R * N + 6 * R * R * P) + nb * 4 * R * P * N)
+        bwd_dbc_flops = units * (2 * pairs * (2 * R * R * P + 2 * R * R * N) + nb * 4 * R * P * N)
     # per-head token gradients (dx, ddt_eff, dl): x, dy, B, C, dS, H_in in; dx out
-    m["chunk_bwd"] = dict(bytes=3 * tokx + 2 * tokbc + 2 * stS + 4 * per_tok,
-                          flops=units * (8 * Q * P * N + 4 * Q * Q * P + 4 * Q * Q * N))
+    m["chunk_bwd"] = dict(bytes=3 * tokx + 2 * tokbc + 2 * stS + 4 * per_tok, flops=bwd_tok_flops)
     # group gradients dB, dC: x, dy, B, C, dS, H_in in; dB, dC out
     m["chunk_bwd_dbc"] = dict(bytes=2 * tokx + 4 * tokbc + 2 * stS + 2 * per_tok,
-                              flops=units * (4 * Q * Q * P + 4 * Q * Q * N + 4 * Q * P * N))
+                              flops=bwd_dbc_flops)
     m["dt_bwd"] = dict(bytes=2 * T * H * s + 4 * per_tok, flops=0)
     m["param_reduce"] = dict(bytes=b * nc * H * 4 * 4, flops=0)
     # compulsory IO of the layer (fwd reads x dt B C, writes y; bwd reads x dt
@@ -86,8 +118,8 @@ def kernel_model(cfg, dtype_bytes):
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
-# one ncu capture of a b2_L8192_bf16 step (profiles/launches_b2_L8192_bf16.md),
-# keyed by kernel, with the sha1 of the sources the kernel was built from: the
+# one ncu capture of a b2_L8192_bf16 step (the committed launch-list
+# summary of that workload), keyed by kernel, with the sha1 of the sources the kernel was built from: the
 # figure is reported only while those sources are unchanged and the workload
 # is the one captured, else null.
 NCU_TRAFFIC_WORKLOAD = "b2_L8192_bf16"
@@ -282,11 +314,13 @@ class OracleSample:
                 f"every row ({self.full.batch} rows, all {self.full.nheads} heads) of {self.name}")
 
 
-def cpu_baseline(name, target_s=15.0, min_s=10.0, single_core_s=4.0):
+def cpu_baseline(name, target_s=15.0, min_s=10.0, single_core_s=4.0, parity_of=None):
     """The oracle on a bounded sample of the workload: a prefix sized to about
     target_s seconds, repeated (whole workload too small) until at least
     min_s seconds of CPU work have been timed, on every host core; then a
-    shorter prefix on one core (``single_core``)."""
+    shorter prefix on one core (``single_core``).  With ``parity_of`` =
+    (inputs, device buffers) the same leg also checks the benched step's
+    outputs against the oracle (``parity``, see oracle_parity)."""
     from oracle import ssd_ref
     smp = OracleSample(name, target_s)
     secs, threads, reps = 0.0, 1, 0
@@ -309,6 +343,8 @@ def cpu_baseline(name, target_s=15.0, min_s=10.0, single_core_s=4.0):
     out["single_core"] = {"value": smp.full.batch * lp1 / t1, "unit": "tokens/s", "cores": th1,
                           "seconds": t1,
                           "sample": f"the first {lp1} tokens of every row, same workload"}
+    if parity_of is not None:
+        out["parity"] = oracle_parity(*parity_of)
     return out
 
 
@@ -365,15 +401,25 @@ def run_gpu(args, world, rank, local):
             mid.record(stream)
         dev.bwd(stream=stream)
 
-    for _ in range(args.warmup):
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1 = torch.cuda.Event(enable_timing=True)
+    for k in range(args.warmup):
+        if k == args.warmup - 1:
+            flush.fill_(0.0)
+            w0.record(stream)
         step()
+    w1.record(stream)
     torch.cuda.synchronize()
     if dev.device_status(stream) != 0:
         raise RuntimeError("device status word reports an error after warm-up")
+    # the timed region runs at least --steps steps and at least MIN_TIMED_S
+    # seconds, so that the clock record under load has enough samples
+    est_ms = max(w0.elapsed_time(w1), 1e-3)
+    nsteps = max(args.steps, int(MIN_TIMED_S * 1e3 / est_ms) + 1)
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps)]
     clocks = ClockSampler(local) if rank == 0 else None
     barrier(world)
     torch.cuda.synchronize()
@@ -382,7 +428,7 @@ def run_gpu(args, world, rank, local):
         time.sleep(0.3)
     _lib.profile_start()
     t_wall0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(nsteps):
         flush.fill_(float(i))
         starts[i].record(stream)
         step(mids[i])
@@ -400,7 +446,7 @@ def run_gpu(args, world, rank, local):
         raise RuntimeError("device status word reports an error in the timed region")
 
     tokens = inp.batch * inp.seqlen
-    value = world * tokens * args.steps / (tot_ms_max / 1e3)
+    value = world * tokens * nsteps / (tot_ms_max / 1e3)
 
     # ---- end to end: pinned host inputs -> device, fwd+bwd, results -> host
     e2e = run_e2e(inp, dev, args, stream)
@@ -444,14 +490,15 @@ def run_gpu(args, world, rank, local):
             d = v["ms_per_launch"] / 1e3
             v["GBps"] = mk["bytes"] / d / 1e9
             v["TFLOPps"] = mk["flops"] / d / 1e12
-    ms_per_step = tot_ms_max / args.steps
-    layer = layer_summary(kernels, model, args.steps, ms_per_step, layer_io, hbm_peak, tc_peak)
+    ms_per_step = tot_ms_max / nsteps
+    layer = layer_summary(kernels, model, nsteps, ms_per_step, layer_io, hbm_peak, tc_peak)
     layer.update(fwd_ms_mean=statistics.mean(fwd_ms),
                  bwd_ms_mean=statistics.mean(t - f for t, f in zip(step_ms, fwd_ms)),
                  step_ms_median=statistics.median(step_ms))
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "steps": nsteps, "steps_requested": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": inp.dtype, "data": "synthetic",
             "config": dict(cfg, l2="flushed between steps (256 MB write, outside the events); "
@@ -459,13 +506,57 @@ def run_gpu(args, world, rank, local):
                            else "single GPU"),
             "roofline": roof, "layer_roofline": layer, "e2e": e2e,
             "gpu_launches": launches, "kernels": kernels, "clocks": clk,
-            "wall_s_timed": t_wall}
+            "wall_s_timed": t_wall,
+            "timed_region": f"{nsteps} steps (at least --steps {args.steps} and at least "
+                            f"{MIN_TIMED_S} s of step time)"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload)
+        base = cpu_baseline(args.workload, parity_of=(inp, dev))
+        line["parity"] = base.pop("parity")
+        line["cpu_baseline"] = base
     return line
 
 
+def oracle_parity(inp, dev):
+    """Part of the oracle leg, after the timed region: the benched step's
+    outputs (the device buffers hold the last step's results) against the
+    float64 oracle on one sampled group of the same inputs -- every batch row,
+    the group's heads, every token -- as max|diff| / max|ref| per tensor."""
+    import numpy as np
+    from oracle import ssd_ref
+    g = int(np.random.default_rng(0).integers(inp.ngroups))
+    hpg = inp.nheads // inp.ngroups
+    hs = slice(g * hpg, (g + 1) * hpg)
+    f = inp.f64
+    t0 = time.perf_counter()
+    init = f("initial_states")
+    ref = ssd_ref.ssd_group(*[f(n) for n in ["x", "dt", "dt_bias", "A", "B", "C", "D"]],
+                            f("dy"), g, inp.ngroups, initial_states=init,
+                            seq_idx=f("seq_idx"), dfinal_states=None,
+                            want_dinit=init is not None)
+    secs = time.perf_counter() - t0
+    got = dev.results()
+    errs = {}
+    for k, r in ref.items():
+        v = got[k].numpy()
+        if k in ("y", "dx", "ddt"):
+            v = v[:, :, hs]
+        elif k in ("final_states", "dinitial_states"):
+            v = v[:, hs]
+        elif k in ("dA", "dD", "ddt_bias"):
+            v = v[hs]
+        else:
+            v = v[:, :, g:g + 1]
+        errs[k] = float(np.abs(v - r).max() / max(np.abs(r).max(), 1e-30))
+    tol = 2e-2 if inp.dtype == "bf16" else 1e-4
+    return {"metric": "max|diff| / max|ref| per tensor", "tolerance": tol,
+            "group": g, "heads": [hs.start, hs.stop], "rel_err": errs,
+            "pass": all(e <= tol for e in errs.values()), "oracle_seconds": secs,
+            "sample": f"group {g} of {inp.ngroups}: every batch row, heads {hs.start}.."
+                      f"{hs.stop - 1}, every token"}
+
+
 E2E_BUFFER_SETS = 3
+MIN_TIMED_S = 1.2
 
 
 def run_e2e(inp, dev, args, stream):

@@ -39,16 +39,21 @@
  *
  * Ownership: the caller allocates every buffer, the workspace included, and
  * keeps them alive until the stream work completes.  The library never
- * allocates, never synchronises (except ssd_read_device_status and
+ * allocates, never synchronises (except the two status readers and
  * ssd_profile_stop) and keeps no mutable global state other than a
- * per-device cache of device attributes and the optional timing records.
+ * per-device cache of device attributes, the optional timing records and
+ * the one exception below: the fixed device array behind ssd_fwd_noalloc
+ * (SSD_NOALLOC_SCRATCH_BYTES on every GPU that loads the library) with a
+ * per-device cache of its address, shared by all ssd_fwd_noalloc calls --
+ * calls of it that overlap on the GPU race on that array (see there).
  * Calls enqueue work on the given stream and return before it completes.
  *
  * Errors: every entry point validates its arguments before enqueuing
  * anything and returns an ssd_status; nothing is thrown across the ABI.
  * Errors detected on the device (a bounded wait that expired) are recorded
  * in a status word at the start of the workspace; read it with
- * ssd_read_device_status.
+ * ssd_read_device_status (ssd_fwd_noalloc_read_device_status for
+ * ssd_fwd_noalloc, whose workspace is the library's own array).
  */
 #ifndef SSD_H_
 #define SSD_H_
@@ -148,12 +153,21 @@ int ssd_read_device_status(const void* workspace, ssd_stream_t stream);
  * stream capture.  All calls share the one array and it keeps the last
  * call's contents (each call re-zeroes what must start at zero): calls that
  * can overlap on the GPU -- on different streams or from different host
- * threads -- race on it. */
+ * threads -- race on it.  Its device status word is read with
+ * ssd_fwd_noalloc_read_device_status. */
 #define SSD_NOALLOC_SCRATCH_BYTES (32u << 20)
 int ssd_fwd_noalloc(const ssd_problem* prob, const void* x, const void* dt, const float* dt_bias,
                     const float* A, const void* B, const void* C, const float* D,
                     const float* initial_states, const int32_t* seq_idx, void* y,
                     float* final_states, ssd_stream_t stream);
+
+/* Status of the last ssd_fwd_noalloc call on the current device: the
+ * counterpart of ssd_read_device_status for the library-owned array, whose
+ * address callers never see.  Synchronises `stream`, then returns SSD_OK or
+ * SSD_ERR_TIMEOUT (a device-side bounded wait of that call expired; its
+ * results are then garbage), or SSD_ERR_CUDA if the synchronisation or the
+ * copy fails.  No counterpart on the pages either. */
+int ssd_fwd_noalloc_read_device_status(ssd_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Gated RMSNorm of the Mamba-2 block: the normalisation the block applies to
@@ -215,7 +229,7 @@ const char* ssd_version(void);
  * stream.  ssd_profile_stop ends recording and waits for the recorded events
  * (it synchronises), folding them into per-kernel totals that
  * ssd_profile_count/ssd_profile_get report (name is a static string).  The
- * event pool holds 8192 launches; ssd_profile_stop returns
+ * event pool holds 32768 launches; ssd_profile_stop returns
  * SSD_ERR_WORKSPACE_TOO_SMALL if launches beyond it went unrecorded.  Use
  * from one host thread. */
 int ssd_profile_start(void);

@@ -32,6 +32,7 @@ SSD_NORM_HAS_Z = 1
 EXPORTS = ["ssd_fwd_workspace_bytes", "ssd_bwd_workspace_bytes", "ssd_fwd", "ssd_bwd",
            "ssd_status_string", "ssd_read_device_status", "ssd_version", "ssd_profile_start",
            "ssd_profile_stop", "ssd_profile_count", "ssd_profile_get", "ssd_fwd_noalloc",
+           "ssd_fwd_noalloc_read_device_status",
            "ssd_gated_rmsnorm_fwd", "ssd_gated_rmsnorm_bwd_workspace_bytes",
            "ssd_gated_rmsnorm_bwd"]
 SSD_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -85,6 +86,8 @@ def _load():
     lib.ssd_profile_get.restype = i32
     lib.ssd_fwd_noalloc.argtypes = [pp] + [vp] * 11 + [vp]
     lib.ssd_fwd_noalloc.restype = i32
+    lib.ssd_fwd_noalloc_read_device_status.argtypes = [vp]
+    lib.ssd_fwd_noalloc_read_device_status.restype = i32
     npp = ctypes.POINTER(ssd_norm_problem)
     lib.ssd_gated_rmsnorm_fwd.argtypes = [npp] + [vp] * 5 + [vp]
     lib.ssd_gated_rmsnorm_fwd.restype = i32
@@ -198,6 +201,11 @@ def ssd_fwd_noalloc(prob, x, dt, dt_bias, A, B, C, D, initial_states, seq_idx, y
     return int(LIB.ssd_fwd_noalloc(ctypes.byref(prob), _p(x), _p(dt), _p(dt_bias), _p(A), _p(B),
                                    _p(C), _p(D), _p(initial_states), _p(seq_idx), _p(y),
                                    _p(final_states), _stream(stream)))
+
+
+def ssd_fwd_noalloc_read_device_status(stream=None) -> int:
+    """Device status word of the last ssd_fwd_noalloc call (synchronises)."""
+    return int(LIB.ssd_fwd_noalloc_read_device_status(_stream(stream)))
 
 
 def make_norm_problem(rows, dim, group_size, eps, dtype, gate=True) -> ssd_norm_problem:

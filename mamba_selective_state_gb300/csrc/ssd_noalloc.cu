@@ -54,3 +54,13 @@ extern "C" int ssd_fwd_noalloc(const ssd_problem* prob, const void* x, const voi
   return ssd_fwd(prob, x, dt, dt_bias, A, B, C, D, initial_states, seq_idx, y, final_states, ws,
                  (size_t)SSD_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+// The status word of the last ssd_fwd_noalloc call sits at the start of the
+// library-owned array, whose address the caller never sees: this reads it
+// there, exactly as ssd_read_device_status reads a caller workspace.
+extern "C" int ssd_fwd_noalloc_read_device_status(ssd_stream_t stream) {
+  void* ws = nullptr;
+  const int rc = ssd::scratch_address(&ws);
+  if (rc != SSD_OK) return rc;
+  return ssd_read_device_status(ws, stream);
+}

@@ -11,7 +11,7 @@ namespace ssd {
 
 namespace {
 
-constexpr int kPoolEvents = 16384;  // two per launch
+constexpr int kPoolEvents = 65536;  // two per launch
 
 struct Rec {
   const char* name;

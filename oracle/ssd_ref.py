@@ -143,6 +143,39 @@ def ssd_bwd(x, dt, dt_bias, A, B, C, D, dy, initial_states=None, seq_idx=None,
     return out
 
 
+def ssd_group(x, dt, dt_bias, A, B, C, D, dy, g, ngroups, initial_states=None, seq_idx=None,
+              dfinal_states=None, want_dinit=True):
+    """Forward and backward restricted to group ``g`` of ``ngroups`` (every
+    batch row, the group's contiguous block of heads, every token).  Each
+    head runs as its own group with a copy of the group's B and C (so the
+    oracle's threads spread over the heads); dB and dC of the group are then
+    the sums of the per-head results in head order.  Returns a dict with y,
+    final_states and the gradients, restricted the same way (dB, dC with a
+    group axis of length 1)."""
+    H = x.shape[2]
+    hpg = H // ngroups
+    hs = slice(g * hpg, (g + 1) * hpg)
+    Bg = np.repeat(np.asarray(B)[:, :, g:g + 1, :], hpg, axis=2)
+    Cg = np.repeat(np.asarray(C)[:, :, g:g + 1, :], hpg, axis=2)
+    init_s = None if initial_states is None else np.asarray(initial_states)[:, hs]
+    dfin_s = None if dfinal_states is None else np.asarray(dfinal_states)[:, hs]
+    args = [np.asarray(x)[:, :, hs], np.asarray(dt)[:, :, hs], np.asarray(dt_bias)[hs],
+            np.asarray(A)[hs], Bg, Cg, np.asarray(D)[hs]]
+    y, fin = ssd_fwd(*args, initial_states=init_s, seq_idx=seq_idx)
+    gr = ssd_bwd(*args, np.asarray(dy)[:, :, hs], initial_states=init_s, seq_idx=seq_idx,
+                 dfinal_states=dfin_s, want_dinit=want_dinit)
+    dB = np.zeros_like(gr["dB"][:, :, :1])
+    dC = np.zeros_like(dB)
+    for k in range(hpg):
+        dB[:, :, 0] += gr["dB"][:, :, k]
+        dC[:, :, 0] += gr["dC"][:, :, k]
+    out = dict(y=y, final_states=fin, dx=gr["dx"], ddt=gr["ddt"], ddt_bias=gr["ddt_bias"],
+               dA=gr["dA"], dD=gr["dD"], dB=dB, dC=dC)
+    if want_dinit:
+        out["dinitial_states"] = gr["dinitial_states"]
+    return out
+
+
 def inputs_f64(inp):
     """Pull the float64 views the oracle needs out of an ``SSDInputs``-like
     object (duck-typed: anything with ``f64(name)``)."""

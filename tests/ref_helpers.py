@@ -24,35 +24,14 @@ def oracle_full(inp, want_dinit=None):
 
 def oracle_group(inp, g):
     """Oracle outputs restricted to group g (every batch row, the group's
-    heads).  Each head runs as its own group with a copy of the group's B, C,
-    so the oracle spreads the heads over its threads; dB and dC of the group
-    are then the sum of the per-head results, taken in head order."""
-    H, G = inp.nheads, inp.ngroups
-    hpg = H // G
-    hs = slice(g * hpg, (g + 1) * hpg)
+    heads, every token); dB and dC of the group sum the per-head results in
+    head order."""
     f = inp.f64
     x, dt, bias, A, B, C, D = [f(n) for n in FWD]
-    Bg = np.repeat(B[:, :, g:g + 1, :], hpg, axis=2)
-    Cg = np.repeat(C[:, :, g:g + 1, :], hpg, axis=2)
     init = f("initial_states")
-    dfin = f("dfinal_states")
-    init_s = None if init is None else init[:, hs]
-    dfin_s = None if dfin is None else dfin[:, hs]
-    args = [x[:, :, hs], dt[:, :, hs], bias[hs], A[hs], Bg, Cg, D[hs]]
-    kw = dict(initial_states=init_s, seq_idx=f("seq_idx"))
-    y, fin = ssd_ref.ssd_fwd(*args, **kw)
-    gr = ssd_ref.ssd_bwd(*args, f("dy")[:, :, hs], dfinal_states=dfin_s,
-                         want_dinit=init is not None, **kw)
-    dB = np.zeros_like(gr["dB"][:, :, :1])
-    dC = np.zeros_like(dB)
-    for k in range(hpg):
-        dB[:, :, 0] += gr["dB"][:, :, k]
-        dC[:, :, 0] += gr["dC"][:, :, k]
-    out = dict(y=y, final_states=fin, dx=gr["dx"], ddt=gr["ddt"], ddt_bias=gr["ddt_bias"],
-               dA=gr["dA"], dD=gr["dD"], dB=dB, dC=dC)
-    if init is not None:
-        out["dinitial_states"] = gr["dinitial_states"]
-    return out
+    return ssd_ref.ssd_group(x, dt, bias, A, B, C, D, f("dy"), g, inp.ngroups,
+                             initial_states=init, seq_idx=f("seq_idx"),
+                             dfinal_states=f("dfinal_states"), want_dinit=init is not None)
 
 
 def slice_group(got, inp, g):

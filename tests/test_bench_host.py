@@ -113,3 +113,23 @@ def test_layer_summary_against_both_roofs():
     assert abs(d["achieved_GBps"] - 2000.0) < 1e-9 and abs(d["frac_of_hbm"] - 0.5) < 1e-12
     assert abs(d["achieved_TFLOPps"] - 2e-6) < 1e-18
     assert abs(d["frac_of_tensor"] - 4e-6) < 1e-18
+
+
+def test_kernel_model_flops_match_a_hand_count():
+    """One chunk of 128 tokens, two heads of one group, headdim 64, d_state
+    32: the matrix products the two backward kernels issue, counted by hand
+    (2 flops per multiply-add)."""
+    cfg = dict(batch=1, seqlen=128, nheads=2, headdim=64, dstate=32, ngroups=1, chunk=128)
+    m, _ = bench.kernel_model(cfg, 2)
+    # token kernel: C B^T once (128x128x32), per head dy x^T (128x128x64),
+    # B dS^T and C H^T (128x64x32 each), M^T dY (128x64x128)
+    cb = 2 * 128 * 128 * 32
+    per_head = 2 * 128 * 128 * 64 + 2 * (2 * 128 * 64 * 32) + 2 * 128 * 64 * 128
+    assert m["chunk_bwd"]["flops"] == cb + 2 * per_head == 11534336
+    # dB/dC kernel, per head: dy x^T, dy H and x dS (128x32x64 each),
+    # dCB B and dCB^T C (128x32x128 each)
+    per_head = 2 * 128 * 128 * 64 + 2 * (2 * 128 * 32 * 64) + 2 * (2 * 128 * 32 * 128)
+    assert m["chunk_bwd_dbc"]["flops"] == 2 * per_head == 10485760
+    # chunk_scan at chunk 128: C B^T and C_rev B^T once, per head A_hat X
+    # (128x64x128) and C H^T (128x64x32)
+    assert m["chunk_scan"]["flops"] == 2 * cb + 2 * (2 * 128 * 64 * 128 + 2 * 128 * 64 * 32)

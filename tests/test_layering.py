@@ -55,8 +55,10 @@ def test_oracle_imports_only_the_input_generators_of_the_package():
 
 
 def test_bench_uses_the_oracle_only_for_cpu_timing():
+    # the oracle leg: CPU timing, and (called from cpu_baseline, after the
+    # timed region) the parity of the benched outputs
     allowed = {"OracleSample.__init__", "OracleSample.run", "cpu_baseline", "run_reference",
-               "norm_oracle_seconds", "run_norm_reference"}
+               "norm_oracle_seconds", "run_norm_reference", "oracle_parity"}
     for mod, fn in _imports(_py(os.path.join(ROOT, "bench.py"))):
         if mod.startswith("oracle"):
             assert fn in allowed, (mod, fn)

@@ -321,3 +321,29 @@ def test_dfinal_only_gradient_is_decay_product():
     x, dt, bias, A = args[:4]
     de = np.log1p(np.exp(dt[0, :, 0] + bias[0]))
     assert rel(g["dinitial_states"][0, 0, 0, 0], np.exp(np.sum(de) * A[0])) < 1e-13
+
+
+def test_group_restriction_equals_full_run():
+    """The group-restricted run (one group's heads, each with a copy of the
+    group's B and C; dB, dC summed over the heads) equals the slice of the
+    full run: heads of other groups do not touch this group's outputs."""
+    inp = make_inputs(batch=2, seqlen=37, nheads=6, headdim=3, dstate=4, ngroups=3, chunk=16,
+                      dtype="f32", init=True, dfinal=True, seq_lengths=[20, 17], seed=4)
+    f = inp.f64
+    args = [f(n) for n in ["x", "dt", "dt_bias", "A", "B", "C", "D"]]
+    kw = dict(initial_states=f("initial_states"), seq_idx=f("seq_idx"))
+    y, fin = ssd_ref.ssd_fwd(*args, **kw)
+    full = ssd_ref.ssd_bwd(*args, f("dy"), dfinal_states=f("dfinal_states"), **kw)
+    for g in range(3):
+        hs = slice(2 * g, 2 * g + 2)
+        got = ssd_ref.ssd_group(*args, f("dy"), g, 3, dfinal_states=f("dfinal_states"), **kw)
+        np.testing.assert_allclose(got["y"], y[:, :, hs], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(got["final_states"], fin[:, hs], rtol=1e-12, atol=1e-14)
+        for k in ("dx", "ddt"):
+            np.testing.assert_allclose(got[k], full[k][:, :, hs], rtol=1e-12, atol=1e-14)
+        for k in ("dA", "dD", "ddt_bias"):
+            np.testing.assert_allclose(got[k], full[k][hs], rtol=1e-12, atol=1e-14)
+        for k in ("dB", "dC"):
+            np.testing.assert_allclose(got[k], full[k][:, :, g:g + 1], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(got["dinitial_states"], full["dinitial_states"][:, hs],
+                                   rtol=1e-12, atol=1e-14)
