@@ -45,9 +45,19 @@ FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=
 # algorithmic bytes and flops per launch: the compulsory reads and writes of
 # each kernel (per-unit figures times the units of one launch)
 # ----------------------------------------------------------------------------
+def eval_chunk(cfg, dtype_bytes):
+    """Chunk length the library evaluates: the tensor-core path (bf16,
+    headdim 64, d_state >= 16, at most 256 heads per group) uses 128-token
+    chunks whatever the problem's chunk_size; otherwise chunk_size."""
+    tc = (dtype_bytes == 2 and cfg["headdim"] == 64 and cfg["dstate"] >= 16
+          and cfg["nheads"] // cfg["ngroups"] <= 256)
+    return 128 if tc else cfg["chunk"]
+
+
 def kernel_model(cfg, dtype_bytes):
-    b, L, H, P, N, G, Q = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate",
-                                             "ngroups", "chunk"))
+    b, L, H, P, N, G = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate",
+                                          "ngroups"))
+    Q = eval_chunk(cfg, dtype_bytes)
     nc = -(-L // Q)
     Lp = nc * Q
     s = dtype_bytes
@@ -65,51 +75,46 @@ def kernel_model(cfg, dtype_bytes):
     m["state_passing_fwd"] = dict(bytes=st32 + stS, flops=2 * units * P * N)
     # the backward's forward pass also keeps the fp32 carry-in states (in place)
     m["state_passing_fwd_keep"] = dict(bytes=2 * st32 + stS, flops=2 * units * P * N)
-    # chunk_scan: per (group, chunk) C B^T over the row/column tile pairs on
-    # or below the diagonal (at chunk 128 also C_rev B^T, the copy with its
-    # row blocks reversed that balances the mask pass); per head
-    # Y1 = A_hat X over the same tile pairs and Y2 = C H_in^T
-    if Q <= 128:
-        scan_cb = (4 if Q == 128 else 2) * Q * Q * N
-        scan_head = 2 * Q * Q * P + 2 * Q * N * P
-    else:
-        R = 128
-        nb = -(-Q // R)
-        pairs = nb * (nb + 1) // 2
-        scan_cb = pairs * 2 * R * R * N
-        scan_head = pairs * 2 * R * R * P + 2 * Q * N * P
+    # chunk_scan: per (group, chunk) C B^T (at chunk 128 also C_rev B^T, the
+    # copy with its row blocks reversed that balances the mask pass); per head
+    # Y1 = A_hat X and Y2 = C H_in^T
+    scan_cb = (4 if Q == 128 else 2) * Q * Q * N
+    scan_head = 2 * Q * Q * P + 2 * Q * N * P
     m["chunk_scan"] = dict(bytes=2 * tokx + 2 * tokbc + stS + 2 * per_tok,
                            flops=gunits * scan_cb + units * scan_head)
     m["chunk_dstate"] = dict(bytes=tokx + tokbc + per_tok + st32, flops=2 * units * Q * P * N)
     # reads dHloc and the fp32 carry-in states (for dL/da_c), writes dS
     m["state_passing_bwd"] = dict(bytes=2 * st32 + stS, flops=4 * units * P * N)
     # Backward flops are counted from the matrix products each kernel issues
-    # (2 flops per multiply-add, dense tiles).  Chunks of up to 128 tokens
-    # (one token tile per chunk): the token kernel forms C B^T once per
-    # group and, per head, dM = dy x^T, dX_s = B dS^T, Y_c = C H_in^T and
-    # dX = M^T dY; the dB/dC kernel, per head, dM again, dC += dy H,
-    # dB += x dS, dC += dCB B and dB += dCB^T C.  Chunks of 256 tokens (two
-    # 128-token tiles, R = 128): per head and per tile pair (I >= J, three
-    # pairs) the token kernel forms C B^T and B C^T, dy x^T and x dy^T and
-    # dX += A_hat dY, plus Y_c and dX_s per diagonal tile; the dB/dC kernel
-    # forms dM and one dCB product per (tile, partner) for dC and for dB
-    # (three pairs each), plus the carry and state products per tile.
-    if Q <= 128:
-        bwd_tok_flops = gunits * 2 * Q * Q * N + units * (4 * Q * Q * P + 4 * Q * P * N)
-        bwd_dbc_flops = units * (2 * Q * Q * P + 4 * Q * N * P + 4 * Q * Q * N)
-    else:
-        R = 128
-        nb = -(-Q // R)
-        pairs = nb * (nb + 1) // 2
-        bwd_tok_flops = units * (pairs * (4 * R * R * N + 6 * R * R * P) + nb * 4 * R * P * N)
-        bwd_dbc_flops = units * (2 * pairs * (2 * R * R * P + 2 * R * R * N) + nb * 4 * R * P * N)
+    # (2 flops per multiply-add, dense tiles): the token kernel forms C B^T
+    # once per group and, per head, dM = dy x^T, dX_s = B dS^T,
+    # Y_c = C H_in^T and dX = M^T dY; the dB/dC kernel, per head, dM again,
+    # dC += dy H, dB += x dS, dC += dCB B and dB += dCB^T C.
+    bwd_tok_flops = gunits * 2 * Q * Q * N + units * (4 * Q * Q * P + 4 * Q * P * N)
+    bwd_dbc_flops = units * (2 * Q * Q * P + 4 * Q * N * P + 4 * Q * Q * N)
     # per-head token gradients (dx, ddt_eff, dl): x, dy, B, C, dS, H_in in; dx out
     m["chunk_bwd"] = dict(bytes=3 * tokx + 2 * tokbc + 2 * stS + 4 * per_tok, flops=bwd_tok_flops)
     # group gradients dB, dC: x, dy, B, C, dS, H_in in; dB, dC out
     m["chunk_bwd_dbc"] = dict(bytes=2 * tokx + 4 * tokbc + 2 * stS + 2 * per_tok,
                               flops=bwd_dbc_flops)
     m["dt_bwd"] = dict(bytes=2 * T * H * s + 4 * per_tok, flops=0)
+    # the backward's state chains, one pass each: forward reads x, B, l, dt_eff
+    # and writes the bf16 carry-in states; reverse reads dy, C, l and the
+    # carry-in states and writes dS (M = 128 rows issued per product)
+    m["state_chain_fwd"] = dict(bytes=tokx + tokbc + 2 * per_tok + stS,
+                                flops=units * 2 * 128 * P * Q)
+    m["state_chain_bwd"] = dict(bytes=tokx + tokbc + per_tok + 2 * stS,
+                                flops=units * (2 * 128 * P * Q + 2 * P * N))
+    # single-pass forward: reads x, dt, B, C (and the initial states), writes
+    # y and the final states; per (row, head, 128-token chunk) it issues C B^T,
+    # C_rev B^T (row blocks 3, 2; balances the mask pass), Y2 = C H_in^T,
+    # S^T = B^T (w.X) (M = 128 rows issued) and Y1 = A_hat X
+    nq = -(-L // 128)
+    fq = 2 * 128 * 128 * N * 2 + 2 * 128 * P * N + 2 * 128 * P * 128 + 2 * 128 * 128 * P
+    m["ssd_fwd_fused"] = dict(bytes=2 * tokx + T * H * s + 2 * tokbc + 2 * b * H * P * N * 4,
+                              flops=b * H * nq * fq)
     m["param_reduce"] = dict(bytes=b * nc * H * 4 * 4, flops=0)
+    m["status_reset"] = dict(bytes=4, flops=0)
     # compulsory IO of the layer (fwd reads x dt B C, writes y; bwd reads x dt
     # B C dy, writes dx ddt dB dC)
     layer_io = (tokx + T * H * s + 2 * tokbc + tokx) + (2 * tokx + T * H * s + 2 * tokbc

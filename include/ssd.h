@@ -88,7 +88,18 @@ enum {
    * (0.1 s with this flag, 2 s otherwise) and the call ends with
    * SSD_ERR_TIMEOUT in the device status word instead of hanging.  Results
    * of such a call are garbage. */
-  SSD_TEST_DROP_SCAN_PUBLISH = 1 << 16
+  SSD_TEST_DROP_SCAN_PUBLISH = 1 << 16,
+  /* Path selection (comparisons and tests; results agree to rounding).  By
+   * default the library takes its single-pass kernels -- in ssd_fwd one
+   * persistent CTA per (batch row, head) that keeps the carry on chip, in
+   * ssd_bwd one such CTA per chain for the forward and the reverse state
+   * chains (bf16, headdim 64, d_state 64 or 128) -- when there are at least
+   * about three chains per four SMs, and otherwise its separate kernels
+   * (chunk cumsum, chunk states, state-passing scan, chunk output).
+   * SSD_PATH_MULTI_KERNEL forces the separate kernels; SSD_PATH_SINGLE_PASS
+   * forces the single-pass kernels wherever their shape set allows. */
+  SSD_PATH_MULTI_KERNEL = 1 << 17,
+  SSD_PATH_SINGLE_PASS = 1 << 18
 };
 
 typedef struct {
@@ -168,6 +179,53 @@ int ssd_fwd_noalloc(const ssd_problem* prob, const void* x, const void* dt, cons
  * results are then garbage), or SSD_ERR_CUDA if the synchronisation or the
  * copy fails.  No counterpart on the pages either. */
 int ssd_fwd_noalloc_read_device_status(ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Context parallelism: the sequence split into contiguous shards (one per
+ * rank, or run one after another on one GPU), each shard run through
+ * ssd_fwd / ssd_bwd as a problem of its own, the shards joined by two
+ * exclusive folds.  Page "B200 Helion Mamba-2" (aitrends.kr/articles/109906)
+ * names context parallelism as the module's integration goal without a
+ * method; it follows from the recurrence: a shard maps the state h entering
+ * it to dec * h + final(0) (dec = product of its per-token decays
+ * exp(dt_eff * A), 0 when a sequence starts after its first token; final(0)
+ * = its final state from a zero start), and its dinitial_states is affine
+ * in the gradient g at its final state, dinit(g) = dec * g + dinit(0).
+ *
+ * Forward: every shard runs from a zero state (its final_states = local),
+ * ssd_shard_decay gives dec and the segment ids of its first and last
+ * tokens; after the exchange of (dec, local, ids) of all shards,
+ * ssd_shard_fold (reverse = 0, boundary = initial_states or NULL) gives the
+ * state entering every shard (out) and the layer's final state (total);
+ * every shard runs again from its entering state.  Backward: every shard's
+ * dinitial_states with no upstream final gradient (local), exchanged,
+ * folded with reverse = 1 (boundary = dfinal_states or NULL) gives every
+ * shard its upstream dfinal_states (out); each shard then runs its backward;
+ * dA, dD and ddt_bias are sums over the shards.  A shard whose first token
+ * starts a new sequence enters from zero and sends no gradient back. */
+
+/* dec (b, H) fp32 of one shard (prob: the shard as a problem; only batch,
+ * seqlen, nheads, dtype and SSD_HAS_SEQ_IDX are read) and, if first_ids /
+ * last_ids (b) int32 are non-NULL (both or neither), the segment ids of the
+ * shard's first and last tokens (0 without seq_idx).  dt (b, Ls, H) dtype;
+ * dt_bias, A (H) fp32; seq_idx (b, Ls) iff SSD_HAS_SEQ_IDX. */
+int ssd_shard_decay(const ssd_problem* prob, const void* dt, const float* dt_bias, const float* A,
+                    const int32_t* seq_idx, float* decay, int32_t* first_ids, int32_t* last_ids,
+                    ssd_stream_t stream);
+
+/* The exclusive fold over nshards shards, in order (reverse = 0) or from
+ * the right (reverse = 1).  decay (R, b, H) fp32; local, out (R, b, H, P, N)
+ * fp32; first_ids, last_ids (R, b) int32 or both NULL (no sequence starts on
+ * shard boundaries); boundary (b, H, P, N) fp32 or NULL (zero); total
+ * (b, H, P, N) fp32 or NULL.  Forward: h = boundary; for r: h = 0 if shard
+ * r > 0 starts a new sequence; out[r] = h; h = decay[r] h + local[r];
+ * total = h.  Reverse: g = boundary; for r = R-1 .. 0: out[r] = g;
+ * g = decay[r] g + local[r]; g = 0 if shard r > 0 starts a new sequence;
+ * total = g.  Device pointers, 16-byte aligned; enqueue only. */
+int ssd_shard_fold(int64_t nshards, int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate,
+                   const float* decay, const float* local, const int32_t* first_ids,
+                   const int32_t* last_ids, const float* boundary, float* out, float* total,
+                   int reverse, ssd_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Gated RMSNorm of the Mamba-2 block: the normalisation the block applies to

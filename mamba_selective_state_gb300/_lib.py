@@ -26,13 +26,15 @@ SSD_HAS_SEQ_IDX = 2
 SSD_HAS_DFINAL = 4
 SSD_WANT_DINIT = 8
 SSD_TEST_DROP_SCAN_PUBLISH = 1 << 16
+SSD_PATH_MULTI_KERNEL = 1 << 17
+SSD_PATH_SINGLE_PASS = 1 << 18
 SSD_NORM_HAS_Z = 1
 
 # every symbol include/ssd.h declares
 EXPORTS = ["ssd_fwd_workspace_bytes", "ssd_bwd_workspace_bytes", "ssd_fwd", "ssd_bwd",
            "ssd_status_string", "ssd_read_device_status", "ssd_version", "ssd_profile_start",
            "ssd_profile_stop", "ssd_profile_count", "ssd_profile_get", "ssd_fwd_noalloc",
-           "ssd_fwd_noalloc_read_device_status",
+           "ssd_fwd_noalloc_read_device_status", "ssd_shard_decay", "ssd_shard_fold",
            "ssd_gated_rmsnorm_fwd", "ssd_gated_rmsnorm_bwd_workspace_bytes",
            "ssd_gated_rmsnorm_bwd"]
 SSD_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -88,6 +90,11 @@ def _load():
     lib.ssd_fwd_noalloc.restype = i32
     lib.ssd_fwd_noalloc_read_device_status.argtypes = [vp]
     lib.ssd_fwd_noalloc_read_device_status.restype = i32
+    lib.ssd_shard_decay.argtypes = [pp] + [vp] * 7 + [vp]
+    lib.ssd_shard_decay.restype = i32
+    i64 = ctypes.c_int64
+    lib.ssd_shard_fold.argtypes = [i64] * 5 + [vp] * 7 + [i32, vp]
+    lib.ssd_shard_fold.restype = i32
     npp = ctypes.POINTER(ssd_norm_problem)
     lib.ssd_gated_rmsnorm_fwd.argtypes = [npp] + [vp] * 5 + [vp]
     lib.ssd_gated_rmsnorm_fwd.restype = i32
@@ -206,6 +213,28 @@ def ssd_fwd_noalloc(prob, x, dt, dt_bias, A, B, C, D, initial_states, seq_idx, y
 def ssd_fwd_noalloc_read_device_status(stream=None) -> int:
     """Device status word of the last ssd_fwd_noalloc call (synchronises)."""
     return int(LIB.ssd_fwd_noalloc_read_device_status(_stream(stream)))
+
+
+def ssd_shard_decay(prob, dt, dt_bias, A, seq_idx, decay, first_ids=None, last_ids=None,
+                    stream=None, check=True) -> int:
+    """One shard's decay (b, H) and the segment ids of its first and last tokens."""
+    rc = LIB.ssd_shard_decay(ctypes.byref(prob), _p(dt), _p(dt_bias), _p(A), _p(seq_idx), _p(decay),
+                             _p(first_ids), _p(last_ids), _stream(stream))
+    if check and rc != SSD_OK:
+        raise SSDError(rc, "ssd_shard_decay")
+    return rc
+
+
+def ssd_shard_fold(decay, local, first_ids, last_ids, boundary, out, total=None, reverse=False,
+                   stream=None, check=True) -> int:
+    """The exclusive fold over the shards (forward or from the right);
+    shapes are read from ``local`` (R, b, H, P, N)."""
+    R, b, H, P, N = local.shape
+    rc = LIB.ssd_shard_fold(R, b, H, P, N, _p(decay), _p(local), _p(first_ids), _p(last_ids),
+                            _p(boundary), _p(out), _p(total), int(bool(reverse)), _stream(stream))
+    if check and rc != SSD_OK:
+        raise SSDError(rc, "ssd_shard_fold")
+    return rc
 
 
 def make_norm_problem(rows, dim, group_size, eps, dtype, gate=True) -> ssd_norm_problem:

@@ -821,23 +821,15 @@ cudaError_t launch_chunk_bwd_group_tc(const Plan& p, const Bufs& f, cudaStream_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_bwd_pair_tc(const Plan& p, const Bufs& f, cudaStream_t s);
-cudaError_t launch_chunk_bwd_dbc_tc(const Plan& p, const Bufs& f, cudaStream_t s);
-bool chunk_bwd_pair_tc_supported(const Plan& p);
+bool chunk_bwd_tc_supported(const Plan& p) { return chunk_bwd_group_tc_supported(p); }
 
-bool chunk_bwd_tc_supported(const Plan& p) {
-  return chunk_bwd_group_tc_supported(p) || chunk_bwd_pair_tc_supported(p);
-}
-
-// Token gradients (per head) then dB, dC (per group).  Chunks of up to 128
-// tokens use the group kernel; 256-token chunks the per-head block-pair kernel.
+// Token gradients (per head) then dB, dC (per group), chunks of up to 128 tokens.
 cudaError_t launch_chunk_bwd_tc(const Plan& p, const Bufs& f, cudaStream_t s) {
-  cudaError_t e = chunk_bwd_group_tc_supported(p) ? launch_chunk_bwd_group_tc(p, f, s)
-                                                  : launch_chunk_bwd_pair_tc(p, f, s);
+  cudaError_t e = launch_chunk_bwd_group_tc(p, f, s);
   if (e != cudaSuccess) return e;
   prof_after(s);  // the entry point brackets one launch; time the second kernel on its own
   prof_before(s);
-  return chunk_bwd_group_tc_supported(p) ? launch_chunk_bwd_dbc_group_tc(p, f, s) : launch_chunk_bwd_dbc_tc(p, f, s);
+  return launch_chunk_bwd_dbc_group_tc(p, f, s);
 }
 
 }  // namespace ssd

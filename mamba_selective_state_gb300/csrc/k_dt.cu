@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Plan p, Bufs f) {
     const float a = f.achunk[bh * p.nc + c];
     if (a != 0.0f) {
       float da = 0.0f;
-      const float* dp = f.dapart + (bh * p.nc + c) * p.sp_neblk;
-      for (int k = 0; k < p.sp_neblk; ++k) da += dp[k];
+      const float* dp = f.dapart + (bh * p.nc + c) * p.da_stride;
+      for (int k = 0; k < p.da_nsum; ++k) da += dp[k];
       extra += a * da;
     }
   }
@@ -204,7 +204,19 @@ __global__ void __launch_bounds__(256) param_reduce_kernel(Plan p, Bufs f) {
   }
 }
 
+// Clears the status word of a call whose kernels do not (the single-pass
+// forward).  A kernel on the call's stream rather than a memset: a memset can
+// be served by a copy engine and queue behind the caller's host copies.
+__global__ void status_reset_kernel(WsHeader* hdr) { hdr->status = 0; }
+
 }  // namespace
+
+cudaError_t launch_status_reset(const Plan& p, const Bufs& f, cudaStream_t s) {
+  (void)p;
+  set_kernel_name("status_reset");
+  status_reset_kernel<<<1, 1, 0, s>>>(f.hdr);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dt_cumsum(const Plan& p, const Bufs& f, cudaStream_t s) {
   set_kernel_name("dt_cumsum");

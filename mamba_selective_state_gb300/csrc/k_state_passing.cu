@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kSpThreads, 3) state_passing_kernel(Plan p, Bu
       const int k = threadIdx.x;
       float d = 0.0f;
       for (int w = 0; w < kSpThreads / 32; ++w) d += s_da[k][w];
-      f.dapart[((size_t)bh * p.nc + chunk_of(k0 + k)) * p.sp_neblk + eblk] = d;
+      f.dapart[((size_t)bh * p.nc + chunk_of(k0 + k)) * p.da_stride + eblk] = d;
     }
   }
   if (active) {

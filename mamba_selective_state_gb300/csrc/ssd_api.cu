@@ -48,7 +48,7 @@ int make_plan(const ssd_problem* pr, Plan* p) {
   if (pr->nheads % pr->ngroups != 0) return SSD_ERR_INVALID_ARGUMENT;
   if (pr->dtype != SSD_F32 && pr->dtype != SSD_BF16) return SSD_ERR_INVALID_ARGUMENT;
   if (pr->flags & ~(SSD_HAS_INIT | SSD_HAS_SEQ_IDX | SSD_HAS_DFINAL | SSD_WANT_DINIT |
-                    SSD_TEST_DROP_SCAN_PUBLISH))
+                    SSD_TEST_DROP_SCAN_PUBLISH | SSD_PATH_MULTI_KERNEL | SSD_PATH_SINGLE_PASS))
     return SSD_ERR_INVALID_ARGUMENT;
   if (pr->chunk_size > 256 || pr->chunk_size % 16 != 0) return SSD_ERR_UNSUPPORTED;
   if (!pow2_in(pr->headdim, 16, 128) || !pow2_in(pr->dstate, 16, 128)) return SSD_ERR_UNSUPPORTED;
@@ -66,8 +66,15 @@ int make_plan(const ssd_problem* pr, Plan* p) {
   p->P = (int)pr->headdim;
   p->N = (int)pr->dstate;
   p->G = (int)pr->ngroups;
-  p->Q = (int)pr->chunk_size;
-  p->nc = (int)nc;
+  // The chunk length is a blocking choice: the chunked evaluation gives the
+  // result of the recurrence for any chunk length (up to rounding).  The
+  // tensor-core path (bf16, headdim 64, d_state 16..128, at most 256 heads
+  // per group) evaluates chunks of 128 tokens, its MMA tile, whatever
+  // chunk_size asks; the CUDA-core path uses chunk_size as given.
+  const bool tc_path = pr->dtype == SSD_BF16 && pr->headdim == 64 && pr->dstate >= 16 &&
+                       pr->nheads / pr->ngroups <= 256;
+  p->Q = tc_path ? 128 : (int)pr->chunk_size;
+  p->nc = (p->L + p->Q - 1) / p->Q;
   p->PN = p->P * p->N;
   p->hpg = p->H / p->G;
   p->dtype = pr->dtype;
@@ -81,6 +88,8 @@ int make_plan(const ssd_problem* pr, Plan* p) {
   // per-chunk partial slots of the chunk-backward kernel: one per chunk on
   // the tensor-core path, one per 32-token block on the CUDA-core path
   p->cb_ntb = chunk_bwd_tc_supported(*p) ? 1 : (p->Q + 31) / 32;
+  p->da_stride = p->sp_neblk > 16 ? p->sp_neblk : 16;
+  p->da_nsum = p->sp_neblk;
 
   const size_t f4 = sizeof(float);
   const size_t bh = (size_t)p->b * p->H;
@@ -104,7 +113,7 @@ int make_plan(const ssd_problem* pr, Plan* p) {
   p->fwd_bytes = off;
   p->off_dS = take(states / 4 * (p->dtype == SSD_BF16 ? 2 : 4));
   p->off_dHl = take(states);
-  p->off_dapart = take(bh * p->nc * p->sp_neblk * f4);
+  p->off_dapart = take(bh * p->nc * p->da_stride * f4);
   p->off_dl = take(bh * p->Lp * f4);
   p->off_ddte = take(bh * p->Lp * f4);
   p->off_udu = take(bh * p->nc * p->cb_ntb * f4);
@@ -147,6 +156,22 @@ int check_device() {
   if (!current_device_info(&d)) return SSD_ERR_CUDA;
   if (d.cc_major != 10 || d.cc_minor != 3) return SSD_ERR_UNSUPPORTED;
   return SSD_OK;
+}
+
+// The single-pass forward runs one CTA per (batch row, head) chain and walks
+// its chunks in order: it is chosen where the shape is in its set and there
+// are chains enough to fill most of the GPU.
+bool enough_chains(const Plan& p) {
+  if (p.flags & SSD_PATH_SINGLE_PASS) return true;
+  return (long long)p.b * p.H * 4 >= (long long)device_sm_count() * 3;
+}
+bool use_fused_fwd(const Plan& p) {
+  if (p.flags & (SSD_PATH_MULTI_KERNEL | SSD_TEST_DROP_SCAN_PUBLISH)) return false;
+  return ssd_fwd_fused_supported(p) && enough_chains(p);
+}
+bool use_state_chains(const Plan& p) {
+  if (p.flags & (SSD_PATH_MULTI_KERNEL | SSD_TEST_DROP_SCAN_PUBLISH)) return false;
+  return state_chain_supported(p) && enough_chains(p);
 }
 
 #define SSD_LAUNCH(expr)                        \
@@ -207,6 +232,12 @@ int ssd_fwd(const ssd_problem* prob, const void* x, const void* dt, const float*
   f.init = initial_states; f.seq = seq_idx; f.y = y; f.final_states = final_states;
   bind_workspace(p, workspace, false, &f);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (use_fused_fwd(p)) {
+    // no scan flags or tickets to reset, only the status word
+    SSD_LAUNCH(launch_status_reset(p, f, s));
+    SSD_LAUNCH(launch_ssd_fwd_fused(p, f, s));
+    return SSD_OK;
+  }
   SSD_LAUNCH(launch_dt_cumsum(p, f, s));
   SSD_LAUNCH(launch_chunk_state(p, f, false, s));
   SSD_LAUNCH(launch_state_passing(p, f, false, false, s));
@@ -249,11 +280,18 @@ int ssd_bwd(const ssd_problem* prob, const void* x, const void* dt, const float*
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // recompute the forward intermediates: dt_eff, chunk cumsums, carry-in states
   SSD_LAUNCH(launch_dt_cumsum(p, f, s));
-  SSD_LAUNCH(launch_chunk_state(p, f, false, s));
-  SSD_LAUNCH(launch_state_passing(p, f, false, true, s));
-  // gradient of the carry-in states from y, then the reverse state-passing scan
-  SSD_LAUNCH(launch_chunk_state(p, f, true, s));
-  SSD_LAUNCH(launch_state_passing(p, f, true, false, s));
+  if (use_state_chains(p)) {
+    // one pass per chain, forward then reverse (16 dL/da_c slots per chunk)
+    p.da_nsum = 16;
+    SSD_LAUNCH(launch_state_chain(p, f, false, s));
+    SSD_LAUNCH(launch_state_chain(p, f, true, s));
+  } else {
+    SSD_LAUNCH(launch_chunk_state(p, f, false, s));
+    SSD_LAUNCH(launch_state_passing(p, f, false, true, s));
+    // gradient of the carry-in states from y, then the reverse state-passing scan
+    SSD_LAUNCH(launch_chunk_state(p, f, true, s));
+    SSD_LAUNCH(launch_state_passing(p, f, true, false, s));
+  }
   SSD_LAUNCH(launch_chunk_bwd(p, f, s));
   SSD_LAUNCH(launch_dt_bwd(p, f, s));
   SSD_LAUNCH(launch_param_reduce(p, f, s));

@@ -41,6 +41,9 @@ struct Plan {
   int sp_neblk, sp_nseg, sp_nseg_b, sp_nslot, sp_chains;  // chains = b * H * neblk; nslot = max segments
   // chunk-backward token blocks per chunk
   int cb_ntb;
+  // dL/da_c partial slots per chunk: da_stride allocated (at least 16),
+  // da_nsum written by the launch that forms them and summed in that order
+  int da_stride, da_nsum;
   // workspace offsets in bytes (0 = absent)
   size_t off_dte, off_lcs, off_achunk;   // (b,H,Lp) f32, (b,H,Lp) f32, (b,H,nc) f32
   // Chunk-state tensors are stored (b, H, nc, N, P): for each state index n a
@@ -53,7 +56,7 @@ struct Plan {
   // backward only
   size_t off_dS;                         // (b,H,nc,N,P) dtype: dL/dS_c
   size_t off_dHl;                        // (b,H,nc,N,P) f32: dL/dH_in[c] from the chunk outputs
-  size_t off_dapart;                     // (b,H,nc,neblk) f32: partial sums of dL/da_c
+  size_t off_dapart;                     // (b,H,nc,da_stride) f32: partial sums of dL/da_c
   size_t off_dl, off_ddte;               // (b,H,Lp) f32 each
   size_t off_udu;                        // (b,H,nc,cb_ntb) f32
   size_t off_pdA, off_pdb;               // (b,nc,H) f32 partials of dA, ddt_bias
@@ -132,6 +135,7 @@ __device__ __forceinline__ int seg_in_of(const Plan& p, const Bufs& f, int bi, i
 
 // Host launchers (each returns the launch's cudaError_t).
 cudaError_t launch_dt_cumsum(const Plan& p, const Bufs& f, cudaStream_t s);
+cudaError_t launch_status_reset(const Plan& p, const Bufs& f, cudaStream_t s);
 // backward: the reverse scan (dS, dinit, dL/da_c partials); keep_f32 (forward
 // only): also keep the fp32 carry-in states, in place over the chunk states.
 cudaError_t launch_state_passing(const Plan& p, const Bufs& f, bool backward, bool keep_f32, cudaStream_t s);
@@ -151,6 +155,15 @@ bool chunk_scan_tc_supported(const Plan& p);
 cudaError_t launch_chunk_scan_tc(const Plan& p, const Bufs& f, cudaStream_t s);
 bool chunk_bwd_tc_supported(const Plan& p);
 cudaError_t launch_chunk_bwd_tc(const Plan& p, const Bufs& f, cudaStream_t s);
+
+// Single-pass forward (one persistent CTA per (batch row, head) chain, the
+// carry kept on chip): bf16, headdim 64, d_state 64 or 128.
+bool ssd_fwd_fused_supported(const Plan& p);
+cudaError_t launch_ssd_fwd_fused(const Plan& p, const Bufs& f, cudaStream_t s);
+// The backward's forward and reverse state chains, one CTA per chain
+// (writes H_in, or dS with dinit and the dL/da_c partials).
+bool state_chain_supported(const Plan& p);
+cudaError_t launch_state_chain(const Plan& p, const Bufs& f, bool reverse, cudaStream_t s);
 
 // Per-kernel timing hooks (ssd_profile.cu): each launcher names the kernel it
 // launches; the entry points bracket every launch with prof_before/after.

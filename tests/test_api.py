@@ -203,7 +203,9 @@ def test_workspace_queries_over_random_shapes(lib):
             assert fw == 0 and bw == 0
             continue
         assert fw > 0 and bw > fw and fw % 256 == 0 and bw % 256 == 0, (b, L, H, P, N, G, Q)
-        longer = lib.make_problem(b, L + Q, H, P, N, G, Q, dt)
+        # a longer sequence by more than any evaluation chunk (the tensor-core
+        # path evaluates 128-token chunks whatever chunk_size asks)
+        longer = lib.make_problem(b, L + 256, H, P, N, G, Q, dt)
         assert lib.ssd_fwd_workspace_bytes(longer) > fw
         rows, gs = int(rng.integers(1, 5000)), 8 * int(rng.integers(1, 65))
         npb = lib.make_norm_problem(rows, gs * G, gs, 1e-5, lib.SSD_BF16, gate=bool(dt))

@@ -77,3 +77,42 @@ def test_reference_arm_prints_once_under_two_ranks():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+CP_WORKER = r"""
+import os, sys, json
+sys.path.insert(0, {root!r})
+import torch, torch.distributed as dist
+dist.init_process_group("gloo")
+from mamba_selective_state_gb300.context_parallel import DistExchange
+ex = DistExchange()
+r = dist.get_rank()
+assert ex.nshards == 2
+g = ex.gather([torch.full((2, 3), float(r + 1))])
+ids = ex.gather([torch.tensor([r, 10 + r], dtype=torch.int32)])
+s = ex.sum(torch.tensor([1.0 + r, 2.0]))
+print(json.dumps({{"rank": r, "g": g.tolist(), "ids": ids.tolist(), "s": s.tolist()}}), flush=True)
+dist.destroy_process_group()
+"""
+
+
+def test_context_parallel_exchange_two_gloo_ranks():
+    """The exchange of the context-parallel driver across two ranks: gathers
+    stack the ranks' parts in rank (= shard) order, for float and int32
+    parts, and the parameter-gradient sum adds the ranks' values."""
+    port = _free_port()
+    procs = []
+    for rank in range(2):
+        env = dict(os.environ, RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE="2",
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), CUDA_VISIBLE_DEVICES="")
+        procs.append(subprocess.Popen([sys.executable, "-c", CP_WORKER.format(root=ROOT)], env=env,
+                                      stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True))
+    outs = []
+    for pr in procs:
+        out, err = pr.communicate(timeout=240)
+        assert pr.returncode == 0, err[-2000:]
+        outs.append(json.loads(out.strip().splitlines()[-1]))
+    for o in outs:
+        assert o["g"] == [[[1.0] * 3] * 2, [[2.0] * 3] * 2]
+        assert o["ids"] == [[0, 10], [1, 11]]
+        assert o["s"] == [3.0, 4.0]

@@ -65,6 +65,10 @@ SMALL = {
                                seq_lengths=[5000, 1, 7806]),
     "fp32_many_segments": dict(batch=1, seqlen=32 * 150, nheads=2, headdim=16, dstate=16,
                                ngroups=1, chunk=32, dtype="f32", init=True, dfinal=True),
+    # sequence starts on chunk boundaries, a one-token sequence, a ragged end
+    "bf16_chunk_aligned_resets": dict(batch=2, seqlen=128 * 5 + 17, nheads=4, headdim=64,
+                                      dstate=128, ngroups=1, chunk=128, dtype="bf16", init=True,
+                                      dfinal=True, seq_lengths=[128, 256, 1, 127, 128, 17]),
     # chunk 32: tensor-core chunk states next to the CUDA-core scan and backward
     "bf16_Q32_mixed": dict(batch=1, seqlen=32 * 9 + 11, nheads=4, headdim=64, dstate=64,
                            ngroups=2, chunk=32, dtype="bf16", init=True, dfinal=True,
@@ -80,6 +84,50 @@ def test_small_parity(name):
     assert_close(got, ref, inp.dtype)
 
 
+# bf16, headdim 64, d_state 64 or 128: the single-pass forward's shape set
+SINGLE_PASS = ["bf16_N128_G2", "bf16_N64_G4_varlen", "bf16_Q256_init", "bf16_single_token",
+               "bf16_shorter_than_chunk", "bf16_Q32_mixed", "bf16_chunk_aligned_resets"]
+
+
+@pytest.mark.parametrize("name", SINGLE_PASS)
+def test_small_parity_single_pass(name):
+    """The single-pass forward (forced on these small problems, which by
+    default take the separate kernels) against the oracle."""
+    from mamba_selective_state_gb300 import _lib
+    inp = make_inputs(seed=3, **SMALL[name])
+    _, got = run_device(inp, extra_flags=_lib.SSD_PATH_SINGLE_PASS)
+    assert_close(got, oracle_full(inp), inp.dtype)
+
+
+def test_single_pass_is_deterministic_and_matches_multi_kernel():
+    from mamba_selective_state_gb300 import _lib
+    from mamba_selective_state_gb300.runner import SSDDevice
+    inp = make_inputs(seed=9, **SMALL["bf16_N64_G4_varlen"])
+    dev = SSDDevice(inp, device="cuda", backward=False, extra_flags=_lib.SSD_PATH_SINGLE_PASS)
+    dev.fwd()
+    torch.cuda.synchronize()
+    y0, f0 = dev.y.clone(), dev.final.clone()
+    dev.fwd()
+    torch.cuda.synchronize()
+    assert torch.equal(dev.y, y0) and torch.equal(dev.final, f0)
+    multi = SSDDevice(inp, device="cuda", backward=False, extra_flags=_lib.SSD_PATH_MULTI_KERNEL)
+    multi.fwd()
+    torch.cuda.synchronize()
+    d = (multi.y.float() - y0.float()).abs().max() / y0.float().abs().max()
+    assert float(d) <= 2e-2
+
+
+def test_single_pass_positive_decay_rate():
+    """A head with A > 0 (a growing state) takes the exact exponential for
+    every entry of the mask (the split decay needs l nonincreasing)."""
+    from mamba_selective_state_gb300 import _lib
+    inp = make_inputs(seed=4, **SMALL["bf16_N128_G2"])
+    inp.A = inp.A.clone()
+    inp.A[1] = 0.01
+    _, got = run_device(inp, extra_flags=_lib.SSD_PATH_SINGLE_PASS)
+    assert_close(got, oracle_full(inp), inp.dtype)
+
+
 def test_null_init_equals_zero_init():
     cfg = dict(SMALL["bf16_N128_G2"])
     cfg["init"] = False
@@ -91,9 +139,11 @@ def test_null_init_equals_zero_init():
         assert torch.equal(got0[k], got1[k]), k
 
 
-def test_backward_is_bitwise_deterministic():
+@pytest.mark.parametrize("single_pass", [False, True])
+def test_backward_is_bitwise_deterministic(single_pass):
+    from mamba_selective_state_gb300 import _lib
     inp = make_inputs(seed=7, **SMALL["bf16_N64_G4_varlen"])
-    dev, a = run_device(inp)
+    dev, a = run_device(inp, extra_flags=_lib.SSD_PATH_SINGLE_PASS if single_pass else 0)
     dev.fwd()
     dev.bwd()
     torch.cuda.synchronize()
