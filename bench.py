@@ -107,10 +107,9 @@ def kernel_model(cfg, dtype_bytes):
                                 flops=units * (2 * 128 * P * Q + 2 * P * N))
     # single-pass forward: reads x, dt, B, C (and the initial states), writes
     # y and the final states; per (row, head, 128-token chunk) it issues C B^T,
-    # C_rev B^T (row blocks 3, 2; balances the mask pass), Y2 = C H_in^T,
-    # S^T = B^T (w.X) (M = 128 rows issued) and Y1 = A_hat X
+    # Y2 = C H_in^T, S^T = B^T (w.X) (M = 128 rows issued) and Y1 = A_hat X
     nq = -(-L // 128)
-    fq = 2 * 128 * 128 * N * 2 + 2 * 128 * P * N + 2 * 128 * P * 128 + 2 * 128 * 128 * P
+    fq = 2 * 128 * 128 * N + 2 * 128 * P * N + 2 * 128 * P * 128 + 2 * 128 * 128 * P
     m["ssd_fwd_fused"] = dict(bytes=2 * tokx + T * H * s + 2 * tokbc + 2 * b * H * P * N * 4,
                               flops=b * H * nq * fq)
     m["param_reduce"] = dict(bytes=b * nc * H * 4 * 4, flops=0)
@@ -420,7 +419,7 @@ def run_gpu(args, world, rank, local):
     # the timed region runs at least --steps steps and at least MIN_TIMED_S
     # seconds, so that the clock record under load has enough samples
     est_ms = max(w0.elapsed_time(w1), 1e-3)
-    nsteps = max(args.steps, int(MIN_TIMED_S * 1e3 / est_ms) + 1)
+    nsteps = max(args.steps, int(args.min_timed_s * 1e3 / est_ms) + 1)
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps)]
@@ -513,7 +512,7 @@ def run_gpu(args, world, rank, local):
             "gpu_launches": launches, "kernels": kernels, "clocks": clk,
             "wall_s_timed": t_wall,
             "timed_region": f"{nsteps} steps (at least --steps {args.steps} and at least "
-                            f"{MIN_TIMED_S} s of step time)"}
+                            f"{args.min_timed_s} s of step time)"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         base = cpu_baseline(args.workload, parity_of=(inp, dev))
         line["parity"] = base.pop("parity")
@@ -802,6 +801,87 @@ def run_norm(args, world, rank, local):
     return line
 
 
+# ----------------------------------------------------------------------------
+# context parallelism of the layer (--op context_parallel)
+# ----------------------------------------------------------------------------
+CP_METRIC = ("SSD layer fwd+bwd tokens/s over a sequence split into context-parallel shards "
+             "(joined by the shard folds)")
+
+
+def run_cp(args, world, rank, local):
+    """The workload's sequence split into --shards equal shards, run one
+    after another on this GPU through the shard driver (every shard twice
+    forward and twice backward, with the decay and fold kernels between),
+    next to the unsharded layer on the same inputs.  On R GPUs the shard
+    passes would run at once; here their sum is timed."""
+    import torch
+    from mamba_selective_state_gb300 import _lib
+    from mamba_selective_state_gb300.context_parallel import (ShardedLayer, StackExchange,
+                                                              shard_bounds, shard_inputs)
+    from mamba_selective_state_gb300.inputs import make_workload
+    from mamba_selective_state_gb300.runner import SSDDevice
+
+    inp = make_workload(args.workload, seed=rank, dfinal=False)
+    R = args.shards
+    L = inp.seqlen
+    sizes = [L // R + (1 if k < L % R else 0) for k in range(R)]
+    shards = [shard_inputs(inp, a, e) for a, e in shard_bounds(L, sizes)]
+    layer = ShardedLayer(shards, list(range(R)), StackExchange(R), device=f"cuda:{local}")
+    dev = SSDDevice(inp, device=f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=f"cuda:{local}")
+
+    def timed(fn, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for i in range(n):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev)
+
+    def sharded():
+        layer.run(initial_states=inp.initial_states, stream=stream)
+
+    def plain():
+        dev.fwd(stream=stream)
+        dev.bwd(stream=stream)
+
+    for _ in range(args.warmup):
+        sharded()
+        plain()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 else None
+    barrier(world)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    _lib.profile_start()
+    tot = timed(sharded, args.steps)
+    prof = _lib.profile_stop()
+    clk = clocks.stop() if clocks else None
+    tot_plain = timed(plain, args.steps)
+    tot = max_over_ranks(world, tot)
+    ms = tot / args.steps
+    tokens = inp.batch * L
+    kernels = {k: {"launches": n, "ms_per_launch": t / n} for k, (n, t) in prof.items()
+               if not k.startswith("_")}
+    return {"op": "context_parallel", "metric": CP_METRIC, "value": world * tokens / (ms / 1e3),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": inp.dtype, "data": "synthetic",
+            "config": dict(workload_config(args.workload), shards=R, shard_tokens=sizes,
+                           execution="shards one after another on one GPU; the exchange is a "
+                                     "stack in one process",
+                           l2="flushed between steps (256 MB write, outside the events)"),
+            "unsharded_ms_per_step": tot_plain / args.steps,
+            "overhead_vs_unsharded": ms / (tot_plain / args.steps),
+            "gpu_launches": sum(v["launches"] for v in kernels.values()), "kernels": kernels,
+            "clocks": clk}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -810,7 +890,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="ssd", choices=["ssd", "gated_rmsnorm"])
+    ap.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S,
+                    help="least step time in the timed region (0: exactly --steps, for profiling)")
+    ap.add_argument("--op", default="ssd", choices=["ssd", "gated_rmsnorm", "context_parallel"])
+    ap.add_argument("--shards", type=int, default=4, help="--op context_parallel: shards")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -828,7 +911,8 @@ def main():
     barrier(world)
     if world > 1 and rank != 0:
         __graft_entry__.build()
-    line = (run_norm if args.op == "gated_rmsnorm" else run_gpu)(args, world, rank, local)
+    run = {"gated_rmsnorm": run_norm, "context_parallel": run_cp}.get(args.op, run_gpu)
+    line = run(args, world, rank, local)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

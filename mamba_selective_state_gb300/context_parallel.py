@@ -118,73 +118,85 @@ def _buffers(inp: SSDInputs, device) -> dict:
     return d
 
 
+class ShardedLayer:
+    """The shards this process owns (``indices``: their places in sequence
+    order), with their device buffers allocated once; ``run`` is one forward
+    and backward of the layer over the whole sequence, joined with the other
+    shards through ``exchange``."""
+
+    def __init__(self, shards: List[SSDInputs], indices: List[int], exchange, device="cuda"):
+        self.own = [_Shard(i, s, _buffers(s, device)) for i, s in zip(indices, shards)]
+        self.exchange = exchange
+        self.device = device
+        s0 = shards[0]
+        self.dims = (s0.batch, s0.nheads, s0.headdim, s0.dstate)
+
+    def run(self, initial_states: Optional[torch.Tensor] = None,
+            dfinal_states: Optional[torch.Tensor] = None, stream=None) -> dict:
+        """Returns, per owned shard, y and the per-token gradients (views of
+        the shard buffers, valid until the next run), and the layer-wide
+        final_states, dA, dD, ddt_bias and dinitial_states (the latter from
+        shard 0, on its owner)."""
+        b, H, P, N = self.dims
+        device, st, exchange = self.device, stream, self.exchange
+        f32 = dict(dtype=torch.float32, device=device)
+        init = None if initial_states is None else initial_states.to(device).contiguous()
+        dfin = None if dfinal_states is None else dfinal_states.to(device).contiguous()
+
+        def fwd(d, prob, init_t):
+            _lib.ssd_fwd(prob, d["x"], d["dt"], d["dt_bias"], d["A"], d["B"], d["C"], d["D"], init_t,
+                         d["seq"], d["y"], d["final"], d["ws"], stream=st)
+
+        def bwd(d, prob, init_t, dfin_t):
+            _lib.ssd_bwd(prob, d["x"], d["dt"], d["dt_bias"], d["A"], d["B"], d["C"], d["D"], init_t,
+                         d["seq"], d["dy"], dfin_t, d["dx"], d["ddt"], d["ddt_bias"], d["dA"], d["dB"],
+                         d["dC"], d["dD"], d["dinit"], d["ws"], stream=st)
+
+        # 1. every owned shard from a zero state, its decay and boundary segment ids
+        for s in self.own:
+            d = s.dev
+            fwd(d, d["prob0"], None)
+            _lib.ssd_shard_decay(d["prob0"], d["dt"], d["dt_bias"], d["A"], d["seq"], d["decay"],
+                                 d["first"], d["last"], stream=st)
+        # 2. exchange, the forward fold, every owned shard again from its entering state
+        FIN0 = exchange.gather([s.dev["final"] for s in self.own])
+        DEC = exchange.gather([s.dev["decay"] for s in self.own])
+        FIRST = exchange.gather([s.dev["first"] for s in self.own])
+        LAST = exchange.gather([s.dev["last"] for s in self.own])
+        R = FIN0.shape[0]
+        enter = torch.empty((R, b, H, P, N), **f32)
+        final = torch.empty((b, H, P, N), **f32)
+        _lib.ssd_shard_fold(DEC, FIN0, FIRST, LAST, init, enter, final, reverse=False, stream=st)
+        for s in self.own:
+            fwd(s.dev, s.dev["prob_init"], enter[s.index])
+        # 3. backward: dinit with no upstream final gradient, the reverse fold,
+        #    then every owned shard's backward with its upstream gradient
+        for s in self.own:
+            bwd(s.dev, s.dev["bprob0"], enter[s.index], None)
+        D0 = exchange.gather([s.dev["dinit"] for s in self.own])
+        gout = torch.empty((R, b, H, P, N), **f32)
+        _lib.ssd_shard_fold(DEC, D0, FIRST, LAST, dfin, gout, None, reverse=True, stream=st)
+        out = dict(final_states=final)
+        for k in ("y", "dx", "ddt", "dB", "dC"):
+            out[k] = {}
+        psum = {k: torch.zeros(H, **f32) for k in ("dA", "dD", "ddt_bias")}
+        for s in self.own:
+            d = s.dev
+            bwd(d, d["bprob"], enter[s.index], gout[s.index])
+            for k in ("y", "dx", "ddt", "dB", "dC"):
+                out[k][s.index] = d[k]
+            for k in psum:
+                psum[k] += d[k]
+            if s.index == 0:
+                out["dinitial_states"] = d["dinit"]
+        for k, v in psum.items():
+            out[k] = exchange.sum(v)
+        return out
+
+
 def run_sharded(shards: List[SSDInputs], indices: List[int], exchange, device="cuda",
                 initial_states: Optional[torch.Tensor] = None,
                 dfinal_states: Optional[torch.Tensor] = None, stream=None) -> dict:
-    """Forward and backward of the layer over a sequence split into shards.
-
-    ``shards`` are the inputs of the shards this process owns (``indices``
-    their places in sequence order), ``exchange`` joins them with the other
-    shards.  Returns, per owned shard, y and the per-token gradients, and the
-    layer-wide final_states, dA, dD, ddt_bias, dinitial_states (the latter
-    from shard 0, valid on its owner)."""
-    own = [_Shard(i, s, _buffers(s, device)) for i, s in zip(indices, shards)]
-    b, H, P, N = shards[0].batch, shards[0].nheads, shards[0].headdim, shards[0].dstate
-    f32 = dict(dtype=torch.float32, device=device)
-    init = None if initial_states is None else initial_states.to(device).contiguous()
-    dfin = None if dfinal_states is None else dfinal_states.to(device).contiguous()
-    st = stream
-
-    def fwd(d, prob, init_t):
-        _lib.ssd_fwd(prob, d["x"], d["dt"], d["dt_bias"], d["A"], d["B"], d["C"], d["D"], init_t,
-                     d["seq"], d["y"], d["final"], d["ws"], stream=st)
-
-    def bwd(d, prob, init_t, dfin_t):
-        _lib.ssd_bwd(prob, d["x"], d["dt"], d["dt_bias"], d["A"], d["B"], d["C"], d["D"], init_t,
-                     d["seq"], d["dy"], dfin_t, d["dx"], d["ddt"], d["ddt_bias"], d["dA"], d["dB"],
-                     d["dC"], d["dD"], d["dinit"], d["ws"], stream=st)
-
-    # 1. every owned shard from a zero state, its decay and boundary segment ids
-    fin0, dec, first, last = [], [], [], []
-    for s in own:
-        d = s.dev
-        fwd(d, d["prob0"], None)
-        _lib.ssd_shard_decay(d["prob0"], d["dt"], d["dt_bias"], d["A"], d["seq"], d["decay"],
-                             d["first"], d["last"], stream=st)
-        fin0.append(d["final"].clone())
-        dec.append(d["decay"].clone())
-        first.append(d["first"].clone())
-        last.append(d["last"].clone())
-    # 2. exchange, the forward fold, every owned shard again from its entering state
-    FIN0, DEC = exchange.gather(fin0), exchange.gather(dec)
-    FIRST, LAST = exchange.gather(first), exchange.gather(last)
-    R = FIN0.shape[0]
-    enter = torch.empty((R, b, H, P, N), **f32)
-    final = torch.empty((b, H, P, N), **f32)
-    _lib.ssd_shard_fold(DEC, FIN0, FIRST, LAST, init, enter, final, reverse=False, stream=st)
-    for s in own:
-        fwd(s.dev, s.dev["prob_init"], enter[s.index])
-    out_y = {s.index: s.dev["y"].clone() for s in own}
-    # 3. backward: dinit with no upstream final gradient, the reverse fold,
-    #    then every owned shard's backward with its upstream gradient
-    d0 = []
-    for s in own:
-        bwd(s.dev, s.dev["bprob0"], enter[s.index], None)
-        d0.append(s.dev["dinit"].clone())
-    D0 = exchange.gather(d0)
-    gout = torch.empty((R, b, H, P, N), **f32)
-    _lib.ssd_shard_fold(DEC, D0, FIRST, LAST, dfin, gout, None, reverse=True, stream=st)
-    out = dict(y=out_y, final_states=final, dx={}, ddt={}, dB={}, dC={})
-    psum = {k: torch.zeros(H, **f32) for k in ("dA", "dD", "ddt_bias")}
-    for s in own:
-        d = s.dev
-        bwd(d, d["bprob"], enter[s.index], gout[s.index])
-        for k in ("dx", "ddt", "dB", "dC"):
-            out[k][s.index] = d[k].clone()
-        for k in psum:
-            psum[k] += d[k]
-        if s.index == 0:
-            out["dinitial_states"] = d["dinit"].clone()
-    for k, v in psum.items():
-        out[k] = exchange.sum(v)
-    return out
+    """One forward and backward of the layer over a sequence split into
+    shards (see ShardedLayer)."""
+    return ShardedLayer(shards, indices, exchange, device).run(initial_states, dfinal_states, stream)

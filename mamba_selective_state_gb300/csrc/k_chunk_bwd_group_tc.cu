@@ -43,8 +43,6 @@ using namespace tc;
 constexpr int kRows = 128;
 constexpr int kCompute = 512;        // 16 compute warps: four read each quarter of the TMEM lanes
 constexpr int kThr = kCompute + 32;   // dB/dC kernel: and one control warp for the copies and MMAs
-constexpr int kThrT = kCompute + 64;  // token kernel: and two control warps (dX; the next head's batch)
-constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kTok = kRows * 128u;  // one (128 tokens x 64) bf16 tile
 
 __host__ __device__ inline uint32_t r1024(uint32_t v) { return (v + 1023u) & ~1023u; }
@@ -83,13 +81,6 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
 }
 
-// Butterfly sum over the 32 lanes, in a fixed order.
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
-}
-
 // Rows beyond a short chunk (chunk < 128) of the x, dy, B and C tiles are
 // never written by the tensor copies: zero them once, so that they add
 // exact zeros wherever a contraction runs over tokens.
@@ -116,380 +107,9 @@ __host__ __device__ inline size_t group_smem_bytes(const GTiles& T, int Q, int h
   return 1024 + T.offF + (size_t)(5 * Q + 24 * kRows + 8) * 4 + 10 * 8 + 16 + (size_t)hpg * 4 + 16;
 }
 
-// Column sums of a 32-row x 8-column block held one row per lane: after the
-// call, lane l holds the sum over the warp's 32 rows of column
-// 4*b4 + 2*b3 + b2 (b_k = bit k of l).  Fixed butterfly order.
-__device__ __forceinline__ float colsum8(float (&v)[8], int lane) {
-  float a4[4];
-  const bool hi16 = lane & 16;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float send = hi16 ? v[k] : v[4 + k];
-    const float keep = hi16 ? v[4 + k] : v[k];
-    a4[k] = keep + __shfl_xor_sync(kFull, send, 16);
-  }
-  float a2[2];
-  const bool hi8 = lane & 8;
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const float send = hi8 ? a4[k] : a4[2 + k];
-    const float keep = hi8 ? a4[2 + k] : a4[k];
-    a2[k] = keep + __shfl_xor_sync(kFull, send, 8);
-  }
-  const bool hi4 = lane & 4;
-  const float send = hi4 ? a2[0] : a2[1];
-  const float keep = hi4 ? a2[1] : a2[0];
-  float a1 = keep + __shfl_xor_sync(kFull, send, 4);
-  a1 += __shfl_xor_sync(kFull, a1, 2);
-  a1 += __shfl_xor_sync(kFull, a1, 1);
-  return a1;
-}
-
 __device__ __forceinline__ void named_sync_compute() {  // the 16 compute warps only
   asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
 }
-
-__global__ void __launch_bounds__(kThrT, 1) chunk_bwd_group_tc_kernel(Plan p, Bufs f,
-                                                                    const __grid_constant__ CUtensorMap tmX,
-                                                                    const __grid_constant__ CUtensorMap tmY,
-                                                                    const __grid_constant__ CUtensorMap tmB,
-                                                                    const __grid_constant__ CUtensorMap tmC,
-                                                                    const __grid_constant__ CUtensorMap tmS,
-                                                                    const __grid_constant__ CUtensorMap tmH) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const GTiles T = gtiles(p.N, p.Q);
-  uint8_t* sB = sm + T.offB;
-  uint8_t* sC = sm + T.offC;
-  uint8_t* sA = sm + T.offA;
-  uint8_t* sXb = sm + T.offX;
-  uint8_t* sYb = sm + T.offY;
-  uint8_t* sS = sm + T.offS;
-  uint8_t* sH = sm + T.offH;
-  float* lq = reinterpret_cast<float*>(sm + T.offF);  // [2 slots][Q] l of a head
-  float* dtq = lq + 2 * p.Q;                          // [2 slots][Q] dt of a head
-  int* sq = reinterpret_cast<int*>(dtq + 2 * p.Q);    // [Q] segment ids
-  float* colR = reinterpret_cast<float*>(sq + p.Q);   // [4 lane quarters][128] column sums of R
-  float* colQ = colR + 4 * kRows;                     // [4][128] column sums of dM (C.B) E
-  float* rowR = colQ + 4 * kRows;                     // [4 warpgroups][128] row sums of R
-  float* carP = rowR + 4 * kRows;                     // [4][128] carry term of dl, by headdim quarter
-  float* duP = carP + 4 * kRows;                      // [4][128] x . dS B, by headdim quarter
-  float* dyxP = duP + 4 * kRows;                      // [4][128] dy . x, by headdim quarter
-  float* red = dyxP + 4 * kRows;                      // [8] per-warp sums
-  // ld_bc, xy[2], sh, b1 (batch 1 done), dx (dX done), mready (M tile written), edone (epilogue read)
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 8);
-  uint64_t *b_bc = bar, *b_xy = bar + 1, *b_sh = bar + 3, *b_b1 = bar + 4, *b_dx = bar + 5, *b_mr = bar + 6,
-           *b_ed = bar + 7;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 8);
-  float* sD = reinterpret_cast<float*>(tmem_slot + 4);  // [hpg] D of the group's heads
-
-  const int c = blockIdx.x, g = blockIdx.y, bi = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const bool ctl = tid >= kCompute;
-  const int wg = (tid >> 7) & 3, r = tid & 127, wq = (tid >> 5) & 3;
-  const int wlane = wq * 32;
-  const int t0 = c * p.Q, len = min(p.Q, p.L - t0);
-  const int hpg = p.hpg, h_first = g * hpg;
-  const long long bh0 = (long long)bi * p.H + h_first;
-  const uint32_t tok_bytes = (uint32_t)T.rows * 128u;
-  const uint32_t c_bytes = (uint32_t)T.ncb * T.rows * T.cw;
-  const uint32_t s_bytes = (uint32_t)p.N * 128u;
-  auto issue_xy = [&](int hh) {
-    const int buf = hh & 1, h = h_first + hh;
-    mbar_expect_tx(&b_xy[buf], 2 * tok_bytes);
-    tma_load_4d(sXb + buf * kTok, &tmX, &b_xy[buf], 0, h, t0, bi);
-    tma_load_4d(sYb + buf * kTok, &tmY, &b_xy[buf], 0, h, t0, bi);
-  };
-  auto issue_sh = [&](int hh) {
-    const int h = h_first + hh;
-    mbar_expect_tx(b_sh, 2 * s_bytes);
-    tma_load_4d(sS, &tmS, b_sh, 0, 0, c, bi * p.H + h);
-    tma_load_4d(sH, &tmH, b_sh, 0, 0, c, bi * p.H + h);
-  };
-  if (tid == kCompute) {  // the control lane starts the tile copies first
-    for (int k = 0; k < 4; ++k) mbar_init(&bar[k], 1);
-    mbar_fence_init();
-    mbar_expect_tx(b_bc, 2 * c_bytes);
-    for (int q = 0; q < T.ncb; ++q) {
-      tma_load_4d(sB + q * T.cblk, &tmB, b_bc, q * 64, g, t0, bi);
-      tma_load_4d(sC + q * T.cblk, &tmC, b_bc, q * 64, g, t0, bi);
-    }
-    issue_xy(0);
-    if (hpg > 1) issue_xy(1);
-    issue_sh(0);
-  }
-  for (int t = tid; t < p.Q; t += kThrT) sq[t] = t < len ? seg_of(p, f, bi, (long long)t0 + t) : -1;
-  if (tid < p.Q) {  // scalars of the group's first head into slot 0
-    lq[tid] = f.lcs[bh0 * p.Lp + t0 + tid];
-    dtq[tid] = f.dte[bh0 * p.Lp + t0 + tid];
-  }
-  for (int k = tid; k < hpg; k += kThrT) sD[k] = f.D[h_first + k];
-  zero_padding(T, sXb, sYb, sB, sC, tid);  // rows the tensor copies never write
-  if (tid == 0) {
-    for (int k = 4; k < 7; ++k) mbar_init(&bar[k], 1);
-    mbar_init(b_ed, 1);
-    mbar_fence_init();
-  }
-  if (tid < 32) tmem_alloc(tmem_slot, 512);
-  fence_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tm = *tmem_slot;
-  // C B^T | dM | dX | dXs (two buffers) | Yc
-  const uint32_t tCB = tm, tDM = tm + 128, tDX = tm + 256, tDXS = tm + 320, tYC = tm + 448;
-  bool ok = true;
-
-  if (ctl) {
-    // ---------------- two control warps; lane 0 of each issues ----------------
-    // warp 0: dX = M^T dy of every head.  warp 1: C B^T, batch 1 (dM, dXs, Yc)
-    // of every head, and the tile copies of the heads after the first two.
-    const int cw = (tid - kCompute) >> 5;
-    if (lane == 0) {
-      const uint32_t id128 = idesc_bf16(128, 128, 0, 0), id64 = idesc_bf16(128, 64, 0, 1);
-      const uint32_t id64t = idesc_bf16(128, 64, 1, 1);
-      auto kdesc_c = [&](const uint8_t* t, int ks) {  // K-major B/C tile, K = d_state
-        const uint32_t kb = (ks * 32) / T.cw, kin = (ks * 32) % T.cw;
-        return smem_desc(smem_u32(t) + kb * T.cblk + kin, 16, 8 * T.cw, T.cswz);
-      };
-      auto kdesc_tok = [&](const uint8_t* t, int ks) {  // K-major 128 x 64 token tile, K = 64
-        return smem_desc(smem_u32(t) + ks * 32, 16, 1024, kSwz128);
-      };
-      auto mndesc_rows = [&](const uint8_t* t, int ks) {  // MN-major (64 wide), K along rows
-        return smem_desc(smem_u32(t) + ks * 16 * 128, 16, 1024, kSwz128);
-      };
-      if (cw == 1) {
-        // batch 1 of head hh: dM = dy x^T, dXs = B dS^T (buffer hh&1), Yc = C H^T
-        auto batch1 = [&](int hh) {
-          const int buf = hh & 1;
-          const uint8_t* sX = sXb + buf * kTok;
-          const uint8_t* sY = sYb + buf * kTok;
-          for (int ks = 0; ks < 4; ++ks) mma_bf16(tDM, kdesc_tok(sY, ks), kdesc_tok(sX, ks), id128, ks > 0);
-          for (int ks = 0; ks < p.N / 16; ++ks) {
-            mma_bf16(tDXS + buf * 64, kdesc_c(sB, ks), mndesc_rows(sS, ks), id64, ks > 0);
-            mma_bf16(tYC, kdesc_c(sC, ks), mndesc_rows(sH, ks), id64, ks > 0);
-          }
-          mma_commit(b_b1);
-        };
-        if (!mbar_wait(b_bc, 0)) ok = false;
-        tc_fence_after();
-        for (int ks = 0; ks < p.N / 16; ++ks)  // C B^T (M = i, N = j, K = d_state), once per group
-          mma_bf16(tCB, kdesc_c(sC, ks), kdesc_c(sB, ks), id128, ks > 0);
-        if (!mbar_wait(&b_xy[0], 0)) ok = false;
-        if (!mbar_wait(b_sh, 0)) ok = false;
-        tc_fence_after();
-        batch1(0);  // its commit also covers C B^T
-        for (int hh = 0; hh + 1 < hpg; ++hh) {
-          const int buf = hh & 1;
-          if (hh >= 1) {  // x, dy of head hh+1 into the buffer head hh-1 used, once its epilogue
-            // has read them (that epilogue waited for the head's MMAs)
-            if (!mbar_wait(b_ed, (hh - 1) & 1)) ok = false;
-            issue_xy(hh + 1);
-          }
-          if (!mbar_wait(b_b1, hh & 1)) ok = false;  // dS, H of head hh+1 once batch 1 of head hh read them
-          issue_sh(hh + 1);
-          // batch 1 of the next head runs under this head's epilogue: dM and Yc of head
-          // hh have been read back; its dXs buffer was last read by the epilogue of head hh-1
-          if (!mbar_wait(b_mr, hh & 1)) ok = false;
-          if (!mbar_wait(&b_xy[buf ^ 1], ((hh + 1) >> 1) & 1)) ok = false;
-          if (!mbar_wait(b_sh, (hh + 1) & 1)) ok = false;
-          tc_fence_after();
-          batch1(hh + 1);
-        }
-      } else {
-        for (int hh = 0; hh < hpg; ++hh) {
-          const int buf = hh & 1;
-          if (!mbar_wait(b_mr, hh & 1)) ok = false;  // M tile of head hh written
-          tc_fence_after();
-          const uint8_t* sY = sYb + buf * kTok;
-          for (int ks = 0; ks < kRows / 16; ++ks) {  // dX = M^T dy (M = j, N = 64, K = tokens i)
-            const uint64_t da = smem_desc(smem_u32(sA) + ks * 16 * 128, kTok, 1024, kSwz128);
-            mma_bf16(tDX, da, mndesc_rows(sY, ks), id64t, ks > 0);
-          }
-          mma_commit(b_dx);
-        }
-      }
-    }
-  } else {
-    // ---------------- 16 compute warps: mask pass and epilogue ----------------
-    const int s_in = seg_in_of(p, f, bi, c);
-    const int s_last = sq[len - 1];
-    const bool one_seg = sq[0] == s_last;  // seq_idx is nondecreasing: no reset inside the chunk
-    const int i = r;  // this thread's row (token) in the mask pass, and its token j in the epilogue
-    const bool tok_ok = i < len;
-    const int si = tok_ok ? sq[i] : -2;
-    const int lim = tok_ok ? i : -1;  // columns j <= lim are on or below the diagonal
-    uint32_t ph_b1 = 0, ph_dx = 0;
-    for (int hh = 0; hh < hpg; ++hh) {
-      const int buf = hh & 1, h = h_first + hh;
-      const long long bh = bh0 + hh;
-      const uint8_t* sX = sXb + buf * kTok;
-      const uint8_t* sY = sYb + buf * kTok;
-      const float* lb = lq + buf * p.Q;
-      const float* db = dtq + buf * p.Q;
-      // scalars of head hh+1 into the other slot (last read by head hh-1, whose
-      // readers all passed the previous iteration's barriers)
-      if (hh + 1 < hpg && tid < p.Q) {
-        cp_async4(lq + (buf ^ 1) * p.Q + tid, f.lcs + (bh + 1) * p.Lp + t0 + tid);
-        cp_async4(dtq + (buf ^ 1) * p.Q + tid, f.dte + (bh + 1) * p.Lp + t0 + tid);
-      }
-      cp_async_commit();
-      if (!mbar_wait(&b_xy[buf], (hh >> 1) & 1)) ok = false;  // x, dy of head hh
-      if (!mbar_wait(b_b1, ph_b1)) ok = false;                // dM, dXs, Yc of head hh
-      ph_b1 ^= 1;
-      tc_fence_after();
-      const float li = tok_ok ? lb[i] : 0.0f;
-      // ---- mask pass: row i, columns 32 wg .. 32 wg + 31 in 8-column steps
-      {
-        float racc = 0.0f;
-        for (int q8 = wg * 4; q8 < wg * 4 + 4; ++q8) {
-          const int j0 = q8 * 8;
-          uint32_t pk[4] = {0, 0, 0, 0};
-          float cr = 0.0f, cq = 0.0f;
-          if (j0 <= wlane + 31 && j0 < len) {  // warp-uniform; else every entry is masked
-            float cb[8], dm[8], rv[8], qv[8];
-            tmem_ld8x2(tmem_addr(tCB, wlane, j0), tmem_addr(tDM, wlane, j0), cb, dm);
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const float4 lj = *reinterpret_cast<const float4*>(lb + j0 + 4 * k);
-              const float4 dj = *reinterpret_cast<const float4*>(db + j0 + 4 * k);
-              int4 sj = make_int4(si, si, si, si);
-              if (!one_seg) sj = *reinterpret_cast<const int4*>(sq + j0 + 4 * k);
-              const float lv[4] = {lj.x, lj.y, lj.z, lj.w}, dv[4] = {dj.x, dj.y, dj.z, dj.w};
-              const int sv[4] = {sj.x, sj.y, sj.z, sj.w};
-              float mv[4];
-#pragma unroll
-              for (int m = 0; m < 4; ++m) {
-                const int e = 4 * k + m;
-                const bool on = j0 + e <= lim && sv[m] == si;
-                const float cbE = cb[e] * __expf(on ? li - lv[m] : -INFINITY);
-                mv[m] = cbE * dv[m];
-                rv[e] = dm[e] * mv[m];
-                qv[e] = dm[e] * cbE;
-                racc += rv[e];
-              }
-              pk[2 * k] = pack2(mv[0], mv[1]);
-              pk[2 * k + 1] = pack2(mv[2], mv[3]);
-            }
-            cr = colsum8(rv, lane);
-            cq = colsum8(qv, lane);
-          }
-          uint8_t* blk = sA + (q8 / 8) * kTok;
-          *reinterpret_cast<uint4*>(blk + swz128_off(i, (q8 % 8) * 8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          if ((lane & 3) == 0) {
-            const int col = j0 + ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-            colR[wq * kRows + col] = cr;
-            colQ[wq * kRows + col] = cq;
-          }
-        }
-        rowR[wg * kRows + i] = racc;
-      }
-      {  // carry term of dl_i: cv_i e^{l_i} dy_i . Yc_i (headdim columns 16 wg .. 16 wg + 15)
-        float yc[16];
-        tmem_ld16(tmem_addr(tYC, wlane, wg * 16), yc);
-        const uint4 a = *reinterpret_cast<const uint4*>(sY + swz128_off(i, wg * 16));
-        const uint4 b = *reinterpret_cast<const uint4*>(sY + swz128_off(i, wg * 16 + 8));
-        const uint32_t dy[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        float s = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float2 d = unpack2(dy[e]);
-          s += d.x * yc[2 * e] + d.y * yc[2 * e + 1];
-        }
-        carP[wg * kRows + i] = (tok_ok && si == s_in) ? __expf(li) * s : 0.0f;
-      }
-      const float w = (tok_ok && sq[i] == s_last) ? __expf(lb[len - 1] - li) : 0.0f;
-      const float u = w * (tok_ok ? db[i] : 0.0f);
-      cp_async_wait_all();  // this thread's scalar copies of head hh+1 have landed
-      fence_async_smem();
-      tc_fence_before();
-      named_sync_compute();  // M tile and partials complete; dM and Yc read back
-      if (tid == 0) {
-        mbar_arrive(b_mr);
-        if (hh > 0) {  // per-chunk sums of head hh-1 (written before this barrier)
-          f.udu[(bh - 1) * p.nc + c] = (red[0] + red[1]) + (red[2] + red[3]);
-          f.pdD[((long long)bi * p.nc + c) * p.H + h - 1] = (red[4] + red[5]) + (red[6] + red[7]);
-        }
-      }
-      // dl and ddt_eff partial sums of this head (token t = r, warpgroup 0)
-      float dl_t = 0.0f, dd_t = 0.0f;
-      if (wg == 0) {
-        const int t = r;
-        dl_t = ((rowR[t] + rowR[kRows + t]) + (rowR[2 * kRows + t] + rowR[3 * kRows + t])) +
-               ((carP[t] + carP[kRows + t]) + (carP[2 * kRows + t] + carP[3 * kRows + t])) -
-               ((colR[t] + colR[kRows + t]) + (colR[2 * kRows + t] + colR[3 * kRows + t]));
-        dd_t = (colQ[t] + colQ[kRows + t]) + (colQ[2 * kRows + t] + colQ[3 * kRows + t]);
-      }
-      if (!mbar_wait(b_dx, ph_dx)) ok = false;  // dX of head hh
-      ph_dx ^= 1;
-      tc_fence_after();
-      // ---- epilogue: token j = r, headdim columns 16 wg .. 16 wg + 15
-      {
-        const int j = r;
-        const float Dh = sD[hh];
-        float du = 0.0f, dyx = 0.0f;
-        __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(f.dx);
-        const long long xrow = (((long long)bi * p.L + t0 + j) * p.H + h) * 64;
-        const int q = wg;
-        float a[16], s[16];
-        tmem_ld16x2(tmem_addr(tDX, wlane, q * 16), tmem_addr(tDXS + buf * 64, wlane, q * 16), a, s);
-        const uint4 x0 = *reinterpret_cast<const uint4*>(sX + swz128_off(j, q * 16));
-        const uint4 x1 = *reinterpret_cast<const uint4*>(sX + swz128_off(j, q * 16 + 8));
-        const uint4 y0 = *reinterpret_cast<const uint4*>(sY + swz128_off(j, q * 16));
-        const uint4 y1 = *reinterpret_cast<const uint4*>(sY + swz128_off(j, q * 16 + 8));
-        const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        const uint32_t ys[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-        uint32_t o[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float2 xv = unpack2(xs[e]), yv = unpack2(ys[e]);
-          du += xv.x * s[2 * e] + xv.y * s[2 * e + 1];
-          dyx += xv.x * yv.x + xv.y * yv.y;
-          o[e] = pack2(a[2 * e] + u * s[2 * e] + Dh * yv.x, a[2 * e + 1] + u * s[2 * e + 1] + Dh * yv.y);
-        }
-        if (tok_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(dx + xrow + q * 16);
-          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-          dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        }
-        duP[wg * kRows + j] = du;
-        dyxP[wg * kRows + j] = tok_ok ? dyx : 0.0f;
-        tc_fence_before();
-        fence_async_smem();  // x and dy are next written by tensor copies (async proxy)
-        named_sync_compute();  // dX, dXs, x, dy of this head read back; du, dy.x partials complete
-        if (tid == 0) mbar_arrive(b_ed);
-        if (wg == 0) {
-          const float du_t = (duP[j] + duP[kRows + j]) + (duP[2 * kRows + j] + duP[3 * kRows + j]);
-          float udu = 0.0f;
-          if (tok_ok) {
-            dd_t += w * du_t;
-            dl_t -= u * du_t;
-            udu = u * du_t;
-            f.ddte[bh * p.Lp + t0 + j] = dd_t;
-            f.dl[bh * p.Lp + t0 + j] = dl_t;
-          }
-          udu = warp_sum(udu);
-          if (lane == 0) red[wq] = udu;
-        } else if (wg == 1) {
-          float v = (dyxP[j] + dyxP[kRows + j]) + (dyxP[2 * kRows + j] + dyxP[3 * kRows + j]);
-          v = warp_sum(v);
-          if (lane == 0) red[4 + wq] = v;
-        }
-      }
-    }
-    named_sync_compute();
-    if (tid == 0) {  // per-chunk sums of the last head
-      const long long bh = bh0 + hpg - 1;
-      f.udu[bh * p.nc + c] = (red[0] + red[1]) + (red[2] + red[3]);
-      f.pdD[((long long)bi * p.nc + c) * p.H + h_first + hpg - 1] = (red[4] + red[5]) + (red[6] + red[7]);
-    }
-  }
-  if (!ok) atomicOr(&f.hdr->status, kDevTimeout);
-  tc_fence_before();
-  __syncthreads();
-  if (tid < 32) tmem_dealloc(tm, 512);
-}
-
 
 // dB, dC of one chunk for one group (chunk <= 128): one CTA per (chunk,
 // group, batch row) accumulates, in tensor memory and in fixed head order,
@@ -522,6 +142,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
   int* sq = reinterpret_cast<int*>(dtq + 2 * p.Q);    // [Q]
   // ld_bc, xy[2], sh, dm (dM done), cs (carry/state MMAs done), dbc (dB/dC MMAs done),
   // scaled (x, dy scaled in place), dcb (dCB tile written; dM read back)
+  float* sfac = reinterpret_cast<float*>(sq + p.Q);   // [3][Q] exp(l_{32 rb} - l_j) dt_j, rb = 1..3
   uint64_t* bar = reinterpret_cast<uint64_t*>(sq + p.Q + 24 * kRows + 8);
   uint64_t *b_bc = bar, *b_xy = bar + 1, *b_sh = bar + 3, *b_dm = bar + 4, *b_cs = bar + 5, *b_dbc = bar + 6,
            *b_sc = bar + 7, *b_dcb = bar + 8;
@@ -658,6 +279,13 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
         cp_async4(dtq + (buf ^ 1) * p.Q + tid, f.dte + bhn * p.Lp + t0 + tid);
       }
       cp_async_commit();
+      // factor table of this head (its scalars are visible since the last
+      // barrier of the previous head, whose mask pass is done with the table);
+      // the barrier after the row scaling orders it before this mask pass
+      if (tid < 3 * p.Q) {
+        const int rb = 1 + tid / p.Q, j = tid % p.Q;
+        sfac[tid] = (j < 32 * rb && j < len) ? __expf(lb[32 * rb] - lb[j]) * db[j] : 0.0f;
+      }
       if (!mbar_wait(&b_xy[buf], (hh >> 1) & 1)) ok = false;  // x, dy of head hh
       if (!mbar_wait(b_dm, ph_dm)) ok = false;                // dM of head hh has read them
       ph_dm ^= 1;
@@ -701,11 +329,27 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
         tc_fence_after();
       }
       {
+        // units strictly below the diagonal block of the warp's 32 rows (one
+        // sequence in the chunk, A_h <= 0): exp(l_i - l_r) exp(l_r - l_j) dt_j
+        // with l_r the l of the block's first row, both factors <= 1, the
+        // second from the table; the others take the exact exponential
+        const bool fact = one_seg && f.A[h_first + hh] <= 0.0f;
         const float li = tok_ok ? lb[i] : 0.0f;
+        const float r_row = wq > 0 ? __expf((tok_ok ? li : lb[len - 1]) - lb[32 * wq]) : 0.0f;
         for (int q = wg * 2; q < wg * 2 + 2; ++q) {
           const int j0 = q * 16;
           uint32_t pk[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-          if (j0 <= wlane + 31 && j0 < len) {  // warp-uniform; else every entry is masked
+          if (j0 <= wlane + 31 && j0 < len && fact && q < 2 * wq) {  // warp-uniform
+            float dm[16];
+            tmem_ld16(tmem_addr(tDM, wlane, j0), dm);
+            const float* sf = sfac + (wq - 1) * p.Q;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float4 sj = *reinterpret_cast<const float4*>(sf + j0 + 4 * k);
+              pk[2 * k] = pack2(dm[4 * k] * sj.x * r_row, dm[4 * k + 1] * sj.y * r_row);
+              pk[2 * k + 1] = pack2(dm[4 * k + 2] * sj.z * r_row, dm[4 * k + 3] * sj.w * r_row);
+            }
+          } else if (j0 <= wlane + 31 && j0 < len) {  // warp-uniform; else every entry is masked
             float dm[16];
             tmem_ld16(tmem_addr(tDM, wlane, j0), dm);
 #pragma unroll
@@ -808,24 +452,16 @@ cudaError_t launch_chunk_bwd_dbc_group_tc(const Plan& p, const Bufs& f, cudaStre
   return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_bwd_group_tc(const Plan& p, const Bufs& f, cudaStream_t s) {
-  set_kernel_name("chunk_bwd_tc");
-  const GTiles T = gtiles(p.N, p.Q);
-  CUtensorMap X, Y, B, C, S, H;
-  if (!group_maps(p, f, &X, &Y, &B, &C, &S, &H)) return cudaErrorInvalidValue;
-  const size_t smem = group_smem_bytes(T, p.Q, p.hpg);
-  cudaError_t e = cudaFuncSetAttribute(chunk_bwd_group_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
-  chunk_bwd_group_tc_kernel<<<dim3(p.nc, p.G, p.b), kThrT, smem, s>>>(p, f, X, Y, B, C, S, H);
-  return cudaGetLastError();
+bool chunk_bwd_tok_tc_supported(const Plan& p);
+cudaError_t launch_chunk_bwd_tok_tc(const Plan& p, const Bufs& f, cudaStream_t s);
+
+bool chunk_bwd_tc_supported(const Plan& p) {
+  return chunk_bwd_group_tc_supported(p) && chunk_bwd_tok_tc_supported(p);
 }
 
-bool chunk_bwd_tc_supported(const Plan& p) { return chunk_bwd_group_tc_supported(p); }
-
-// Token gradients (per head) then dB, dC (per group), chunks of up to 128 tokens.
+// Token gradients (per head; k_chunk_bwd_tok_tc.cu) then dB, dC (per group).
 cudaError_t launch_chunk_bwd_tc(const Plan& p, const Bufs& f, cudaStream_t s) {
-  cudaError_t e = launch_chunk_bwd_group_tc(p, f, s);
+  cudaError_t e = launch_chunk_bwd_tok_tc(p, f, s);
   if (e != cudaSuccess) return e;
   prof_after(s);  // the entry point brackets one launch; time the second kernel on its own
   prof_before(s);

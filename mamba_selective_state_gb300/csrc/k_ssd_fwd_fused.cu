@@ -20,22 +20,25 @@
 // the chunked evaluation (page "llm-mamba-200", sections 1-3); the chunk
 // length is internal to this kernel (the result does not depend on it).
 //
-// Warp roles (576 threads):
+// Warp roles (608 threads):
 //   warps 0-15  compute: per chunk the carry update, the masked A_hat tile, the
 //               weighted copy w . X of the next chunk and the y epilogue; warp w
 //               reads TMEM lane quarter w % 4 (its SM sub-partition)
 //   warp 16     control: one lane issues every TMA copy and every tcgen05.mma
-//   warp 17     scalars: softplus, the chunk cumsum, decays and sequence
-//               resets of the chunks ahead, into a ring of three slots
-// The mask pass is balanced over the lane quarters as in the chunk-scan
-// kernel: a second product C_rev B^T (C's row blocks 3 and 2 in lane
-// quarters 0 and 1) lets the light quarters take part of the heavy row
-// blocks, so every quarter does five 16-column units.  Units strictly below
+//   warps 17-18 scalars: softplus, the chunk cumsum, decays and sequence
+//               resets of the chunks ahead (even and odd chunks), into a ring
+//               of three slots
+// Lane quarter q holds rows 32q..32q+31 of the chunk and so the 2q+2
+// 16-column units of A_hat on or below the diagonal.  Units strictly below
 // the diagonal block of their 32-row block factor the decay as
 // exp(l_i - l_r) exp(l_r - l_j) with l_r the l of the block's first row:
 // both factors are <= 1 (l is nonincreasing when A_h <= 0), so the
 // per-column factors are a table formed once per chunk and the unit needs
-// two multiplies per entry instead of an exponential.
+// two multiplies per entry instead of an exponential; the heavy quarters'
+// extra units are of this kind, the two diagonal units of every quarter take
+// the exact exponential.  (Shared-memory bandwidth, shared by the tensor
+// core's operand reads and the warps, bounds this kernel: a second product
+// to balance the quarters would cost more operand traffic than it saves.)
 #include "ssd_internal.cuh"
 #include "tc_common.cuh"
 #include "tma_host.h"
@@ -49,20 +52,21 @@ using namespace tc;
 constexpr int kQ = 128;               // tokens per chunk = MMA M
 constexpr int kCompute = 512;         // 16 compute warps
 constexpr int kCtl = kCompute;        // first thread of the control warp
-constexpr int kScal = kCompute + 32;  // first thread of the scalar warp
-constexpr int kThr = kCompute + 64;
+constexpr int kScal = kCompute + 32;  // first thread of the two scalar warps
+constexpr int kThr = kCompute + 96;
 constexpr int kRing = 3;              // scalar slots
 constexpr int kXbuf = 3;              // x tiles (the epilogue stages y in them)
 
 // One scalar slot: per token l, dt_eff, w, cve (= cv exp(l)), the factor
 // tables s[rb-1][j] = exp(l_{32 rb} - l_j) dt_eff_j (j < 32 rb) of row blocks
-// 1..3, the segment ids, and per chunk a_c, one_seg, len, exp-free flag and
+// 1..3 and sd[j] = exp(l_{32 (j/32)} - l_j) dt_eff_j (j's own block), the
+// segment ids, and per chunk a_c, one_seg, len, the two factoring flags and
 // the reference l of each row block.
 struct alignas(16) Slot {
-  float l[kQ], dte[kQ], w[kQ], cve[kQ], s[3][kQ];
+  float l[kQ], dte[kQ], w[kQ], cve[kQ], s[3][kQ], sd[kQ];
   int sq[kQ];
   float a_c;
-  int one_seg, len, fact;
+  int one_seg, len, fact, fact_diag;
   float lref[4];
 };
 
@@ -71,23 +75,19 @@ __host__ __device__ inline uint32_t r1024(uint32_t v) { return (v + 1023u) & ~10
 struct FusedGeom {
   int ncb;          // 64-column blocks of B/C along d_state
   uint32_t cblk;    // bytes of one B/C column block (kQ rows x 128 B)
-  uint32_t crblk;   // bytes of one C_rev column block (64 rows x 128 B)
-  uint32_t offX, offB, offC, offCr, offXs, offA, offH, offSl, offBar, bytes;
+  uint32_t offX, offB, offC, offXs, offA, offH, offSl, offBar, bytes;
 };
 
 __host__ __device__ inline FusedGeom fused_geom(int N) {
   FusedGeom g;
   g.ncb = N / 64;
   g.cblk = kQ * 128u;
-  g.crblk = 64u * 128u;
   g.offX = 0;
   g.offB = g.offX + kXbuf * g.cblk;
+  // with d_state 64 the product B^T (w . X) reads a second (unused) 64-row
+  // block of A past the B tile: the C tile
   g.offC = g.offB + g.ncb * g.cblk;
-  g.offCr = g.offC + g.ncb * g.cblk;
-  // the C_rev MMA reads 128 rows from each column block start: rows 64..127
-  // (garbage for lane quarters 2, 3, which are never read) run into the next
-  // column block and, for the last one, into the w . X tile
-  g.offXs = g.offCr + g.ncb * g.crblk;
+  g.offXs = g.offC + g.ncb * g.cblk;
   g.offA = g.offXs + g.cblk;
   g.offH = g.offA + 2u * g.cblk;
   g.offSl = g.offH + r1024((uint32_t)N * 128u);
@@ -155,11 +155,27 @@ __device__ __forceinline__ void unit_fact(const float (&v)[16], const float* s, 
   }
 }
 
+// Factored unit inside the row block's own 32-column diagonal block (every
+// block's decay range at most e^80, so sd_j = exp(l_r - l_j) dt_j stays
+// finite): (C_tok . B_j) * r * sd_j for j <= tok, else 0.
+__device__ __forceinline__ void unit_fact_diag(const float (&v)[16], const float* sd, int j0, int lim, float r,
+                                               uint32_t (&pk)[8]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 sj = *reinterpret_cast<const float4*>(sd + j0 + 4 * k);
+    const float sv[4] = {sj.x, sj.y, sj.z, sj.w};
+    float a[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) a[m] = j0 + 4 * k + m <= lim ? v[4 * k + m] * sv[m] * r : 0.0f;
+    pk[2 * k] = pack_bf16x2(a[0], a[1]);
+    pk[2 * k + 1] = pack_bf16x2(a[2], a[3]);
+  }
+}
+
 __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
                                                                 const __grid_constant__ CUtensorMap tmX,
                                                                 const __grid_constant__ CUtensorMap tmB,
                                                                 const __grid_constant__ CUtensorMap tmC,
-                                                                const __grid_constant__ CUtensorMap tmC32,
                                                                 const __grid_constant__ CUtensorMap tmY) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -171,7 +187,6 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
   uint8_t* sX = sm + G.offX;     // [kXbuf] x tiles; y is staged in place
   uint8_t* sB = sm + G.offB;
   uint8_t* sC = sm + G.offC;
-  uint8_t* sCr = sm + G.offCr;   // C row blocks 3, 2 (64 rows)
   uint8_t* sXs = sm + G.offXs;   // w . X
   uint8_t* sA = sm + G.offA;     // A_hat, two 64-column blocks
   uint8_t* sH = sm + G.offH;     // carry-in state, (d_state rows, 64 bf16)
@@ -199,7 +214,6 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
-    prefetch_tmap(&tmC32);
     prefetch_tmap(&tmY);
   }
   if (warp == 0) tmem_alloc(tmem_slot, 512);
@@ -207,7 +221,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tmem_slot;
-  const uint32_t tCB = tm, tCBr = tm + 128, tS = tm + 256, tY1 = tm + 320, tY2 = tm + 384;  // tY2: [2] x 64
+  const uint32_t tCB = tm, tS = tm + 128, tY1 = tm + 192, tY2 = tm + 256;  // tY2: [2] x 64
   bool ok = true;
 
   if (warp == kCtl / 32) {
@@ -220,12 +234,10 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
         tma_load_4d(sX + k * G.cblk, &tmX, &b_x[k], 0, h, c * kQ, bi);
       };
       auto load_bc = [&](int c) {
-        mbar_expect_tx(b_bc, G.ncb * (2u * G.cblk + G.crblk));
+        mbar_expect_tx(b_bc, G.ncb * 2u * G.cblk);
         for (int q = 0; q < G.ncb; ++q) {
           tma_load_4d(sB + q * G.cblk, &tmB, b_bc, q * 64, g, c * kQ, bi);
           tma_load_4d(sC + q * G.cblk, &tmC, b_bc, q * 64, g, c * kQ, bi);
-          for (int rb = 0; rb < 2; ++rb)  // C_rev rows 32 rb.. = C rows 32 (3 - rb)..
-            tma_load_4d(sCr + q * G.crblk + rb * 32 * 128, &tmC32, b_bc, q * 64, g, c * kQ + 32 * (3 - rb), bi);
         }
       };
       const uint32_t id128 = idesc_bf16(128, 128, 0, 0);  // K-major A and B
@@ -241,15 +253,13 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
         wait_or_flag(b_hin, ph, ok);
         wait_or_flag(b_xs, ph, ok);
         tc_fence_after();
-        // group 1: C B^T, C_rev B^T, S^T = B^T (w . X), Y2 = C H_in^T
+        // group 1: C B^T, S^T = B^T (w . X), Y2 = C H_in^T
         for (int ks = 0; ks < p.N / 16; ++ks) {
           const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
           const uint64_t dc = smem_desc(smem_u32(sC) + kb * G.cblk + kin, 16, 1024, kSwz128);
-          const uint64_t dcr = smem_desc(smem_u32(sCr) + kb * G.crblk + kin, 16, 1024, kSwz128);
           const uint64_t db = smem_desc(smem_u32(sB) + kb * G.cblk + kin, 16, 1024, kSwz128);
           const uint64_t dh = smem_desc(smem_u32(sH) + ks * 2048, 16, 1024, kSwz128);
           mma_bf16(tCB, dc, db, id128, ks > 0);
-          mma_bf16(tCBr, dcr, db, id128, ks > 0);
           mma_bf16(tY2 + ph * 64, dc, dh, id64b, ks > 0);
         }
         for (int ks = 0; ks < kQ / 16; ++ks) {
@@ -270,7 +280,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
             load_x(c + 2);
           }
         }
-        wait_or_flag(b_m1, ph, ok);  // B, C, C_rev and w . X are free
+        wait_or_flag(b_m1, ph, ok);  // B, C and w . X are free
         if (c + 1 < nch) load_bc(c + 1);
         wait_or_flag(b_ahat, ph, ok);
         tc_fence_after();
@@ -289,7 +299,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
       bulk_wait_all();
       wait_or_flag(b_y, (nch - 1) & 1, ok);  // the last products have completed
     }
-  } else if (warp == kScal / 32) {
+  } else if (warp >= kScal / 32) {
     // ------------------------------ scalars ------------------------------
     const float bias = f.dt_bias[h], Ah = f.A[h];
     const bool fact_ok = Ah <= 0.0f;  // l nonincreasing: both factors of a split decay are <= 1
@@ -309,14 +319,16 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
         }
       }
     };
+    // scalar warp sw fills the slots of chunks sw, sw + 2, ...
+    const int sw = warp - kScal / 32;
     float raw[4];
     int sg[4];
-    load_raw(0, raw, sg);
-    for (int c = 0; c < nch; ++c) {
+    load_raw(sw, raw, sg);
+    for (int c = sw; c < nch; c += 2) {
       const int slot = c % kRing;
       float rawn[4];
       int sgn[4];
-      load_raw(c + 1, rawn, sgn);  // next chunk's loads in flight during this one
+      load_raw(c + 2, rawn, sgn);  // this warp's next chunk: loads in flight during this one
       const int t0 = c * kQ, len = min(kQ, p.L - t0);
       float de[4], lv[4], run = 0.0f;
 #pragma unroll
@@ -344,8 +356,12 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
         seg_first = __ldg(seqr + t0);
       }
       float lref[4];
+      bool diag_ok = true;  // every 32-token block spans a decay of e^80 or less
 #pragma unroll
-      for (int rb = 0; rb < 4; ++rb) lref[rb] = __shfl_sync(0xffffffffu, lv[0], 8 * rb);
+      for (int rb = 0; rb < 4; ++rb) {
+        lref[rb] = __shfl_sync(0xffffffffu, lv[0], 8 * rb);
+        diag_ok = diag_ok && (lref[rb] - __shfl_sync(0xffffffffu, lv[3], 8 * rb + 7) <= 80.0f);
+      }
       if (c >= kRing) {
         bool okw = true;
         wait_or_flag(&b_empty[slot], ((c / kRing) - 1) & 1, okw);
@@ -365,12 +381,14 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
 #pragma unroll
         for (int rb = 1; rb < 4; ++rb)
           S.s[rb - 1][j] = (in && j < 32 * rb) ? __expf(lref[rb] - lv[k]) * de[k] : 0.0f;
+        S.sd[j] = (in && diag_ok) ? __expf(lref[lane >> 3] - lv[k]) * de[k] : 0.0f;
       }
       if (lane == 0) {
         S.a_c = (seg_last == seg_in) ? expf(l_last) : 0.0f;
         S.one_seg = (seg_first == seg_last) ? 1 : 0;
         S.len = len;
         S.fact = (fact_ok && seg_first == seg_last) ? 1 : 0;
+        S.fact_diag = (S.fact && diag_ok) ? 1 : 0;
 #pragma unroll
         for (int rb = 0; rb < 4; ++rb) S.lref[rb] = lref[rb];
       }
@@ -407,24 +425,25 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
       __syncwarp();
       if (lane == 0) mbar_arrive(b);
     };
-    // w . X of chunk c: thread -> row tid/4, two 16-byte pieces (the tile's
-    // swizzle permutes pieces within a row, so the copy keeps the layout)
+    // w . X of chunk c: warp w scales rows 8 w .. 8 w + 7, 8 lanes per
+    // 128-byte row (conflict-free; the tile's swizzle permutes the 16-byte
+    // pieces within a row, so the scaled copy keeps the layout)
     auto scale_x = [&](int c) {
       const Slot& S = ring[c % kRing];
       wait_or_flag(&b_full[c % kRing], (c / kRing) & 1, ok);
       wait_or_flag(&b_x[c % kXbuf], (c / kXbuf) & 1, ok);
-      const int row = tid >> 2, part = tid & 3;
-      const float wv = S.w[row];
-      const uint4* src = reinterpret_cast<const uint4*>(sX + (c % kXbuf) * G.cblk + row * 128) + part * 2;
-      uint4* dst = reinterpret_cast<uint4*>(sXs + row * 128) + part * 2;
+      const uint4* src = reinterpret_cast<const uint4*>(sX + (c % kXbuf) * G.cblk);
+      uint4* dst = reinterpret_cast<uint4*>(sXs);
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint4 v = src[q];
-        v.x = scale_bf16x2(v.x, wv);
-        v.y = scale_bf16x2(v.y, wv);
-        v.z = scale_bf16x2(v.z, wv);
-        v.w = scale_bf16x2(v.w, wv);
-        dst[q] = v;
+      for (int it = 0; it < 2; ++it) {
+        const int r = 8 * warp + 4 * it + (lane >> 3), e = r * 8 + (lane & 7);
+        const float wr = S.w[r];
+        uint4 v = src[e];
+        v.x = scale_bf16x2(v.x, wr);
+        v.y = scale_bf16x2(v.y, wr);
+        v.z = scale_bf16x2(v.z, wr);
+        v.w = scale_bf16x2(v.w, wr);
+        dst[e] = v;
       }
       fence_async_smem();
       arrive(b_xs);
@@ -441,8 +460,6 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
       *reinterpret_cast<uint4*>(blk + swz128_off(n, e0 + 8)) = make_uint4(0, 0, 0, 0);
     }
     scale_x(0);
-    const int lo = sq4 < 2 ? sq4 : 3 - sq4, hi = 3 - lo;
-    const int nlo = 2 * lo + 2, split = 5 - nlo;
     for (int c = 0; c < nch; ++c) {
       const int slot = c % kRing;
       const Slot& S = ring[slot];
@@ -465,33 +482,21 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
       fence_async_smem();
       tc_fence_before();
       arrive(b_hin);
-      // ---- A_hat: balanced mask pass (five 16-column units per lane quarter)
+      // ---- A_hat: row 32 sq4 + lane, the 2 sq4 + 2 units on or below the diagonal
       {
         const int len = S.len;
-        for (int u = wg; u < 5; u += 4) {
-          int rb, q;
-          bool rev = false;
-          if (sq4 == lo) {
-            if (u < nlo) {
-              rb = lo;
-              q = u;
-            } else {
-              rb = hi;
-              q = u - nlo;
-              rev = true;
-            }
-          } else {
-            rb = hi;
-            q = split + u;
-          }
-          const int tok = rb * 32 + lane;
+        const int tok = n;
+        const bool tok_ok = tok < len;
+        const float r_row = __expf(S.l[tok] - S.lref[sq4]);
+        for (int q = wg; q <= 2 * sq4 + 1; q += 4) {
           uint32_t pk[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-          if (q * 16 < len) {
+          if (q * 16 < len) {  // warp-uniform
             float v[16];
-            tmem_ld16(tmem_addr(rev ? tCBr : tCB, 32 * sq4, q * 16), v);
-            const bool tok_ok = tok < len;
-            if (S.fact && q < 2 * rb) {
-              unit_fact(v, S.s[rb - 1], q * 16, __expf(S.l[tok] - S.lref[rb]), pk);
+            tmem_ld16(tmem_addr(tCB, 32 * sq4, q * 16), v);
+            if (S.fact && q < 2 * sq4) {
+              unit_fact(v, S.s[sq4 - 1], q * 16, r_row, pk);
+            } else if (S.fact_diag) {  // diagonal block, factored within it
+              unit_fact_diag(v, S.sd, q * 16, tok_ok ? tok : -1, r_row, pk);
             } else {
               unit_exact(v, S, q * 16, tok_ok ? tok : -1, tok_ok ? S.sq[tok] : -2, S.l[tok], pk);
             }
@@ -505,7 +510,8 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
       fence_async_smem();
       tc_fence_before();
       arrive(b_ahat);
-      // ---- w . X of the next chunk (its tile landed long since)
+      // ---- w . X of the next chunk (the products of this chunk have read the
+      // tile: the carry update above waited for them)
       if (c + 1 < nch) scale_x(c + 1);
       // ---- epilogue: y = Y1 + cv e^l Y2 + D x, staged in place of x
       wait_or_flag(b_y, c & 1, ok);
@@ -553,24 +559,22 @@ bool ssd_fwd_fused_supported(const Plan& p) {
 cudaError_t launch_ssd_fwd_fused(const Plan& p, const Bufs& f, cudaStream_t s) {
   set_kernel_name("ssd_fwd_fused");
   const FusedGeom G = fused_geom(p.N);
-  CUtensorMap tmX, tmB, tmC, tmC32, tmY;
+  CUtensorMap tmX, tmB, tmC, tmY;
   const uint64_t dxx[4] = {64, (uint64_t)p.H, (uint64_t)p.L, (uint64_t)p.b};
   const uint64_t sxx[3] = {128, (uint64_t)p.H * 128, (uint64_t)p.L * p.H * 128};
   const uint32_t bxx[4] = {64, 1, (uint32_t)kQ, 1};
   const uint64_t dbc[4] = {(uint64_t)p.N, (uint64_t)p.G, (uint64_t)p.L, (uint64_t)p.b};
   const uint64_t sbc[3] = {(uint64_t)p.N * 2, (uint64_t)p.G * p.N * 2, (uint64_t)p.L * p.G * p.N * 2};
   const uint32_t bbc[4] = {64, 1, (uint32_t)kQ, 1};
-  const uint32_t bbc32[4] = {64, 1, 32, 1};
   if (!encode_tmap_bf16_4d(&tmX, f.x, dxx, sxx, bxx, 128) ||
       !encode_tmap_bf16_4d(&tmB, f.B, dbc, sbc, bbc, 128) ||
       !encode_tmap_bf16_4d(&tmC, f.C, dbc, sbc, bbc, 128) ||
-      !encode_tmap_bf16_4d(&tmC32, f.C, dbc, sbc, bbc32, 128) ||
       !encode_tmap_bf16_4d(&tmY, f.y, dxx, sxx, bxx, 128))
     return cudaErrorInvalidValue;
   const size_t smem = 1024 + G.bytes;
   cudaError_t e = cudaFuncSetAttribute(ssd_fwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  ssd_fwd_fused_kernel<<<p.b * p.H, kThr, smem, s>>>(p, f, tmX, tmB, tmC, tmC32, tmY);
+  ssd_fwd_fused_kernel<<<p.b * p.H, kThr, smem, s>>>(p, f, tmX, tmB, tmC, tmY);
   return cudaGetLastError();
 }
 

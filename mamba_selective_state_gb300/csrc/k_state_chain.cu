@@ -168,23 +168,37 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
 #pragma unroll
       for (int k = 0; k < 16; ++k) v[k] = (src != nullptr && nvalid) ? src[(bh * p.P + p0 + k) * p.N + n] : 0.0f;
     }
-    // w . T1 of step k: thread -> row tid/4, two 16-byte pieces (the tile's
-    // swizzle permutes pieces within a row, so the scaled copy keeps it)
-    auto scale = [&](int k) {
-      const int s = k % kStages, c = chunk_of(k);
-      const int t0 = c * kQ, len = min(kQ, p.L - t0);
-      const int row = tid >> 2, part = tid & 3;
-      float wv = 0.0f;
-      if (row < len) {
-        const int sr = seqr ? __ldg(seqr + t0 + row) : 0;
-        if (kRev) {
-          const int s_in = seqr ? __ldg(seqr + (t0 > 0 ? t0 - 1 : 0)) : 0;
-          if (sr == s_in) wv = expf(__ldg(lrow + t0 + row));
-        } else {
-          const int s_last = seqr ? __ldg(seqr + t0 + len - 1) : 0;
-          if (sr == s_last) wv = expf(__ldg(lrow + t0 + len - 1) - __ldg(lrow + t0 + row)) * __ldg(drow + t0 + row);
+    // The per-token weight of this thread's row in step k, from scalars
+    // loaded two steps ahead (their latency hides behind two chunks of work).
+    struct Raw {
+      float l, lref, d;
+      int s, sref;
+      bool in;
+    };
+    auto ld_raw = [&](int k) {
+      Raw r{0.0f, 0.0f, 0.0f, 0, 0, false};
+      if (k < nc) {
+        const int c = chunk_of(k), t0 = c * kQ, len = min(kQ, p.L - t0), row = tid >> 2;
+        r.in = row < len;
+        if (r.in) {
+          r.l = __ldg(lrow + t0 + row);
+          r.d = __ldg(drow + t0 + row);
+          r.lref = kRev ? 0.0f : __ldg(lrow + t0 + len - 1);
+          r.s = seqr ? __ldg(seqr + t0 + row) : 0;
+          r.sref = seqr ? __ldg(seqr + (kRev ? (t0 > 0 ? t0 - 1 : 0) : t0 + len - 1)) : 0;
         }
       }
+      return r;
+    };
+    auto make_w = [&](const Raw& r) {
+      if (!r.in || r.s != r.sref) return 0.0f;
+      return kRev ? expf(r.l) : expf(r.lref - r.l) * r.d;
+    };
+    // w . T1 of step k: thread -> row tid/4, two 16-byte pieces (the tile's
+    // swizzle permutes pieces within a row, so the scaled copy keeps it)
+    auto scale = [&](int k, float wv) {
+      const int s = k % kStages;
+      const int row = tid >> 2, part = tid & 3;
       wait_or_flag(&b_ld[s], (k / kStages) & 1, ok);
       const uint4* src = reinterpret_cast<const uint4*>(sm + s * G.stage + row * 128) + part * 2;
       uint4* dst = reinterpret_cast<uint4*>(sXs + (k & 1) * G.blk + row * 128) + part * 2;
@@ -201,9 +215,27 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
       __syncwarp();
       if (lane == 0) mbar_arrive(&b_xs[k & 1]);
     };
-    scale(0);
+    // reverse: this thread's 16 carry-in values of the next chunk, loaded one
+    // chunk ahead (they only enter dL/da_c)
+    auto load_h = [&](int k, uint4 (&hv)[2]) {
+      hv[0] = hv[1] = make_uint4(0, 0, 0, 0);
+      if (kRev && hwarp && nvalid && k < nc) {
+        const uint4* hp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(f.Hin) +
+                                                         ((bh * nc + chunk_of(k)) * p.N + n) * 64 + p0);
+        hv[0] = hp[0];
+        hv[1] = hp[1];
+      }
+    };
+    uint4 hcur[2];
+    load_h(0, hcur);
+    Raw rnext = ld_raw(1);
+    scale(0, make_w(ld_raw(0)));
     for (int k = 0; k < nc; ++k) {
-      if (k + 1 < nc) scale(k + 1);
+      uint4 hnext[2];
+      load_h(k + 1, hnext);
+      const Raw r2 = ld_raw(k + 2);
+      if (k + 1 < nc) scale(k + 1, make_w(rnext));
+      rnext = r2;
       const int c = chunk_of(k), b = k & 1;
       const float a = f.achunk[bh * nc + c];
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(kRev ? f.dS : f.Hin) + ((bh * nc + c) * p.N + n) * 64 + p0;
@@ -215,10 +247,8 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
         reinterpret_cast<uint4*>(out)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
         reinterpret_cast<uint4*>(out)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
         if (kRev) {  // dL/da_c partial: <G, H_in[c]> over this thread's 16 entries
-          const uint4* hp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(f.Hin) +
-                                                           ((bh * nc + c) * p.N + n) * 64 + p0);
-          const uint4 h0 = hp[0], h1 = hp[1];
-          const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+          const uint32_t hw[8] = {hcur[0].x, hcur[0].y, hcur[0].z, hcur[0].w,
+                                  hcur[1].x, hcur[1].y, hcur[1].z, hcur[1].w};
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[e]));
@@ -242,6 +272,8 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&b_free[b]);
+      hcur[0] = hnext[0];
+      hcur[1] = hnext[1];
     }
     if (kRev && f.dinit != nullptr && nvalid) {
 #pragma unroll

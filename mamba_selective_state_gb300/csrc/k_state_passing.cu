@@ -16,9 +16,9 @@
 // (dS goes to its own buffer; dHloc is read once).
 // The backward is the same scan run over the chunks in reverse order.
 //
-// Decomposition.  A tile is (row b, head h, a block of 1024 consecutive state
+// Decomposition.  A tile is (row b, head h, a block of 512 consecutive state
 // elements, a segment of consecutive chunks: 16 forward, 8 in reverse).  One
-// thread issues bulk asynchronous copies of the segment's chunk blocks (4 KB
+// thread issues bulk asynchronous copies of the segment's chunk blocks (2 KB
 // each; in reverse also the fp32 carry-in states) into shared memory, so the
 // whole segment is in flight at once without holding registers; each thread
 // then owns 4 consecutive elements (one float4, conflict-free in shared

@@ -87,7 +87,9 @@ int make_plan(const ssd_problem* pr, Plan* p) {
   p->sp_chains = p->b * p->H * p->sp_neblk;
   // per-chunk partial slots of the chunk-backward kernel: one per chunk on
   // the tensor-core path, one per 32-token block on the CUDA-core path
-  p->cb_ntb = chunk_bwd_tc_supported(*p) ? 1 : (p->Q + 31) / 32;
+  // per-chunk partial slots of the chunk-backward kernel: one per warp row
+  // block on the tensor-core path, one per 32-token block on the CUDA-core path
+  p->cb_ntb = chunk_bwd_tc_supported(*p) ? 4 : (p->Q + 31) / 32;
   p->da_stride = p->sp_neblk > 16 ? p->sp_neblk : 16;
   p->da_nsum = p->sp_neblk;
 

@@ -133,3 +133,18 @@ def test_kernel_model_flops_match_a_hand_count():
     # chunk_scan at chunk 128: C B^T and C_rev B^T once, per head A_hat X
     # (128x64x128) and C H^T (128x64x32)
     assert m["chunk_scan"]["flops"] == 2 * cb + 2 * (2 * 128 * 64 * 128 + 2 * 128 * 64 * 32)
+
+
+def test_kernel_model_single_pass_forward_is_the_compulsory_io():
+    """The single-pass forward's algorithmic bytes are exactly the forward's
+    compulsory IO (x, dt, B, C in; y out) plus the two state tensors; the
+    tensor-core path's evaluation chunk is 128 whatever chunk_size asks."""
+    cfg = dict(batch=2, seqlen=1000, nheads=8, headdim=64, dstate=128, ngroups=2, chunk=256)
+    assert bench.eval_chunk(cfg, 2) == 128 and bench.eval_chunk(cfg, 4) == 256
+    m, _ = bench.kernel_model(cfg, 2)
+    T = 2 * 1000
+    io = 2 * T * 8 * 64 * 2 + T * 8 * 2 + 2 * T * 2 * 128 * 2 + 2 * 2 * 8 * 64 * 128 * 4
+    assert m["ssd_fwd_fused"]["bytes"] == io
+    # per (row, head, 128-token chunk): C B^T, C H^T, S^T (128 rows issued), A_hat X
+    per = 2 * 128 * 128 * 128 + 2 * 128 * 64 * 128 + 2 * 128 * 64 * 128 + 2 * 128 * 128 * 64
+    assert m["ssd_fwd_fused"]["flops"] == 2 * 8 * 8 * per
