@@ -128,18 +128,11 @@ def kernel_model(cfg, dtype_bytes):
 # is the one captured, else null.
 NCU_TRAFFIC_WORKLOAD = "b2_L8192_bf16"
 NCU_TRAFFIC = {
-    "chunk_bwd_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.337e+08, "6c4e7c1bf87e51993efe579775ecaa4c493f5b31"),
-    "chunk_bwd_dbc_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.643e+08, "6c4e7c1bf87e51993efe579775ecaa4c493f5b31"),
-    "chunk_scan_tc": (('k_chunk_scan_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.553e+08, "93ea9b99f762e1d29de0b41a8f939b752458acac"),
-    "chunk_state_tc": (('k_chunk_state_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.852e+08, "df92163105b60f19eb51171ba07e76d9b980c645"),
-    "chunk_dstate_tc": (('k_chunk_state_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.797e+08, "df92163105b60f19eb51171ba07e76d9b980c645"),
-    "state_passing_fwd": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 3.973e+08, "e329d09e0456a47222a119dfafa261e087eebd75"),
-    "state_passing_fwd_keep": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.331e+08, "e329d09e0456a47222a119dfafa261e087eebd75"),
-    "state_passing_bwd": (('k_state_passing.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.541e+08, "e329d09e0456a47222a119dfafa261e087eebd75"),
-    # the gated RMSNorm after the same workload's scan (bench.py --op gated_rmsnorm)
-    "gated_norm_fwd": (('k_gated_norm.cu', 'ssd_internal.cuh'), 3.657e+08, "f587d4f32953c50ce64efc0fc949b0aebeecf91f"),
-    "gated_norm_bwd": (('k_gated_norm.cu', 'ssd_internal.cuh'), 6.303e+08, "f587d4f32953c50ce64efc0fc949b0aebeecf91f"),
-    "gated_norm_dw_fold": (('k_gated_norm.cu', 'ssd_internal.cuh'), 3.743e+06, "f587d4f32953c50ce64efc0fc949b0aebeecf91f"),
+    "ssd_fwd_fused": (('k_ssd_fwd_fused.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 2.9970e+08, "b16be78c71fd7435a0f4f5b86e36dcb3cdc661dc"),
+    "state_chain_fwd": (('k_state_chain.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 2.6800e+08, "9c431e45b6a0bf4bf86d6b595f0b93a4644d03e0"),
+    "state_chain_bwd": (('k_state_chain.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.0690e+08, "9c431e45b6a0bf4bf86d6b595f0b93a4644d03e0"),
+    "chunk_bwd_tc": (('k_chunk_bwd_tok_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.4550e+08, "9a3ecf98171ff223164b5e67b9d9cb5e6a554aa2"),
+    "chunk_bwd_dbc_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.6575e+08, "00ec6d1d14077fb773bd26a1258f597bd139117a"),
 }
 
 

@@ -111,7 +111,8 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
                                                                  const __grid_constant__ CUtensorMap tmB,
                                                                  const __grid_constant__ CUtensorMap tmC,
                                                                  const __grid_constant__ CUtensorMap tmS,
-                                                                 const __grid_constant__ CUtensorMap tmH) {
+                                                                 const __grid_constant__ CUtensorMap tmH,
+                                                                 const __grid_constant__ CUtensorMap tmDX) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const TokGeom T = tok_geom(p.N);
@@ -212,8 +213,15 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
           wait(b_sh, hh & 1);
           if (hh >= 1) {
             // the epilogue of head hh-1 has read dXs, Yc and its x, dy buffer
+            // and left that head's dx in the dy tile: store it, then refill
+            // the buffer once the store has read it
             wait(b_ed, (hh - 1) & 1);
-            if (hh + 1 < hpg) issue_xy(hh + 1);
+            tma_store_4d(&tmDX, sYb + ((hh - 1) & 1) * kTok, 0, h_first + hh - 1, t0, bi);
+            bulk_commit();
+            if (hh + 1 < hpg) {
+              bulk_wait_read<0>();
+              issue_xy(hh + 1);
+            }
           }
           tc_fence_after();
           for (int ks = 0; ks < p.N / 16; ++ks) {
@@ -226,6 +234,10 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
             issue_sh(hh + 1);
           }
         }
+        wait(b_ed, (hpg - 1) & 1);  // the last head's dx
+        tma_store_4d(&tmDX, sYb + ((hpg - 1) & 1) * kTok, 0, h_first + hpg - 1, t0, bi);
+        bulk_commit();
+        bulk_wait_all();
       } else {
         // ---------------- control B: per head Z = M^T dY, W = M X ----------------
         for (int hh = 0; hh < hpg; ++hh) {
@@ -363,13 +375,24 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
         const uint8_t* sY = sYb + buf * kTok;
         const uint32_t tz = tZW + buf * 128, tw = tz + 64;
         // the accumulator rows in two halves (Z, dXs for dx; then W, Yc), so that
-        // no more than 32 of them are live at once
-        float z[16], s16[16];
-        tmem_ld16x2(tmem_addr(tz, wlane, wg * 16), tmem_addr(tDXS, wlane, wg * 16), z, s16);
+        // no more than 32 of them are live at once; the first half's reads are
+        // in flight while the x, dy rows come from shared memory
+        uint32_t zr[16], sr[16];
+        tmem_ld16_issue(tmem_addr(tz, wlane, wg * 16), zr);
+        tmem_ld16_issue(tmem_addr(tDXS, wlane, wg * 16), sr);
+        uint4* y0p = reinterpret_cast<uint4*>(const_cast<uint8_t*>(sY) + swz128_off(t, wg * 16));
+        uint4* y1p = reinterpret_cast<uint4*>(const_cast<uint8_t*>(sY) + swz128_off(t, wg * 16 + 8));
         const uint4 x0 = *reinterpret_cast<const uint4*>(sX + swz128_off(t, wg * 16));
         const uint4 x1 = *reinterpret_cast<const uint4*>(sX + swz128_off(t, wg * 16 + 8));
-        const uint4 y0 = *reinterpret_cast<const uint4*>(sY + swz128_off(t, wg * 16));
-        const uint4 y1 = *reinterpret_cast<const uint4*>(sY + swz128_off(t, wg * 16 + 8));
+        const uint4 y0 = *y0p;
+        const uint4 y1 = *y1p;
+        tmem_ld_wait2(zr, sr);
+        float z[16], s16[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          z[k] = __uint_as_float(zr[k]);
+          s16[k] = __uint_as_float(sr[k]);
+        }
         const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         const uint32_t ys[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
         const float dtt = tv ? db[t] : 0.0f;
@@ -398,12 +421,10 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
             ca = fmaf(yv.x, y16[2 * k], fmaf(yv.y, y16[2 * k + 1], ca));
           }
         }
-        if (tv) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(f.dx) +
-                                                (((long long)bi * p.L + t0 + t) * p.H + h) * 64 + wg * 16);
-          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-          dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        }
+        // dx in place of this thread's dy row piece (already read), for the
+        // tensor store of the whole tile (rows past the sequence are clipped)
+        *y0p = make_uint4(o[0], o[1], o[2], o[3]);
+        *y1p = make_uint4(o[4], o[5], o[6], o[7]);
         pZX[wg * kQ + t] = zx;
         pWY[wg * kQ + t] = wy;
         pDU[wg * kQ + t] = du;
@@ -456,7 +477,7 @@ bool chunk_bwd_tok_tc_supported(const Plan& p) {
 cudaError_t launch_chunk_bwd_tok_tc(const Plan& p, const Bufs& f, cudaStream_t s) {
   set_kernel_name("chunk_bwd_tc");
   const TokGeom T = tok_geom(p.N);
-  CUtensorMap X, Y, B, C, S, H;
+  CUtensorMap X, Y, B, C, S, H, DX;
   const uint64_t dbc[4] = {(uint64_t)p.N, (uint64_t)p.G, (uint64_t)p.L, (uint64_t)p.b};
   const uint64_t sbc[3] = {(uint64_t)p.N * 2, (uint64_t)p.G * p.N * 2, (uint64_t)p.L * p.G * p.N * 2};
   const uint32_t bbc[4] = {(uint32_t)(T.cw / 2), 1, (uint32_t)kQ, 1};
@@ -468,12 +489,13 @@ cudaError_t launch_chunk_bwd_tok_tc(const Plan& p, const Bufs& f, cudaStream_t s
   const uint32_t bs[4] = {64, (uint32_t)p.N, 1, 1};
   if (!encode_tmap_bf16_4d(&X, f.x, dxx, sxx, bxx, 128) || !encode_tmap_bf16_4d(&Y, f.dy, dxx, sxx, bxx, 128) ||
       !encode_tmap_bf16_4d(&B, f.B, dbc, sbc, bbc, T.cw) || !encode_tmap_bf16_4d(&C, f.C, dbc, sbc, bbc, T.cw) ||
-      !encode_tmap_bf16_4d(&S, f.dS, ds, ss, bs, 128) || !encode_tmap_bf16_4d(&H, f.Hin, ds, ss, bs, 128))
+      !encode_tmap_bf16_4d(&S, f.dS, ds, ss, bs, 128) || !encode_tmap_bf16_4d(&H, f.Hin, ds, ss, bs, 128) ||
+      !encode_tmap_bf16_4d(&DX, f.dx, dxx, sxx, bxx, 128))
     return cudaErrorInvalidValue;
   const size_t smem = tok_smem_bytes(T, p.hpg);
   cudaError_t e = cudaFuncSetAttribute(chunk_bwd_tok_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  chunk_bwd_tok_tc_kernel<<<dim3(p.nc, p.G, p.b), kThr, smem, s>>>(p, f, X, Y, B, C, S, H);
+  chunk_bwd_tok_tc_kernel<<<dim3(p.nc, p.G, p.b), kThr, smem, s>>>(p, f, X, Y, B, C, S, H, DX);
   return cudaGetLastError();
 }
 

@@ -517,13 +517,23 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
       wait_or_flag(b_y, c & 1, ok);
       tc_fence_after();
       {
-        float a[16], b[16];
-        tmem_ld16x2(tmem_addr(tY1, 32 * sq4, p0), tmem_addr(tY2 + (c & 1) * 64, 32 * sq4, p0), a, b);
+        // the accumulator reads are in flight while the x row comes from
+        // shared memory
+        uint32_t ar[16], br[16];
+        tmem_ld16_issue(tmem_addr(tY1, 32 * sq4, p0), ar);
+        tmem_ld16_issue(tmem_addr(tY2 + (c & 1) * 64, 32 * sq4, p0), br);
         const float cv = S.cve[n];
         uint8_t* xt = sX + (c % kXbuf) * G.cblk;
         uint4* x0p = reinterpret_cast<uint4*>(xt + swz128_off(n, p0));
         uint4* x1p = reinterpret_cast<uint4*>(xt + swz128_off(n, p0 + 8));
         const uint4 x0 = *x0p, x1 = *x1p;
+        tmem_ld_wait2(ar, br);
+        float a[16], b[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          a[k] = __uint_as_float(ar[k]);
+          b[k] = __uint_as_float(br[k]);
+        }
         const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         uint32_t o[8];
 #pragma unroll

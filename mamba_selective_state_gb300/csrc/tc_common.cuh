@@ -234,6 +234,11 @@ __device__ __forceinline__ void tmem_ld8x2(uint32_t ta, uint32_t tb, float (&a)[
     b[i] = __uint_as_float(r[8 + i]);
   }
 }
+// Wait for the loads issued into a and b (16 registers each) by
+// tmem_ld16_issue; the registers pass through the wait.
+__device__ __forceinline__ void tmem_ld_wait2(uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : SSD_R16(a, 0), SSD_R16(b, 0)::"memory");
+}
 #undef SSD_R16
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
   return base + (lane << 16) + col;
