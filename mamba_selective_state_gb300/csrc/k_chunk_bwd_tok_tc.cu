@@ -26,15 +26,21 @@
 // TMA, TMEM and warp specialisation on Blackwell; the derivation of the
 // reverse mode is this library's, from the recurrence.)
 //
-// One CTA per (chunk, group, batch row): 16 compute warps (warp w reads TMEM
-// lane quarter w % 4) and two control warps, one lane of each issuing.
-//   control A: the tile copies, C B^T once, per head dXs = B dS^T, Yc = C H^T;
-//   control B: per head Z = M^T dY and W = M X into a double-buffered pair;
-//   compute, per head hh: the M tile (units strictly below a row block's
+// A work unit is one (chunk, group, batch row); a persistent CTA per SM takes
+// units blockIdx.x, blockIdx.x + gridDim.x, ... and walks the heads of its
+// units as one sequence, so the copies and products of a unit's first head
+// overlap the last heads of the unit before.  16 compute warps (warp w reads
+// TMEM lane quarter w % 4) and two control warps, one lane of each issuing:
+//   control A: the B, C, dS, H copies, C B^T once per unit, per head
+//     dXs = B dS^T and Yc = C H^T (as soon as the previous head's epilogue
+//     has read them);
+//   control B: the x, dy copies, per head Z = M^T dY and W = M X into a
+//     double-buffered pair, the dx stores;
+//   compute, per head: the M tile (units strictly below a row block's
 //     diagonal block use exp(l_i - l_r) exp(l_r - l_j) dt_j, l_r the block's
 //     first row, both exponentials <= 1, the second from a per-head table),
-//     then the epilogue of head hh-1 while the tensor core forms Z, W of
-//     head hh.
+//     then the epilogue of the previous head while the tensor core forms Z, W
+//     of this one.
 // Per-token results leave through fixed-order folds of the four warpgroups'
 // partial dot products; the per-chunk sums through fixed warp butterflies.
 #include "ssd_internal.cuh"
@@ -80,13 +86,15 @@ __host__ __device__ inline TokGeom tok_geom(int N) {
   return t;
 }
 
-// floats after offF: l, dt [3 slots][Q]; segment ids [Q]; factor table
-// [3][Q]; five partial arrays [4][Q]; per-warp sums [8]; then the barriers,
-// the TMEM address and D of the group's heads
-constexpr int kFloats = 3 * kQ + 3 * kQ + kQ + 3 * kQ + 20 * kQ + 8;
+// floats after offF: l, dt [3 slots][Q]; segment ids [4 units][Q]; unit
+// table [4][8]; factor table [3][Q];
+// five partial arrays [4][Q]; per-warp sums [8]; then the barriers and the
+// TMEM address
+constexpr int kRingU = 4;  // units whose segment ids and coordinates are kept
+constexpr int kFloats = 3 * kQ + 3 * kQ + kRingU * kQ + kRingU * 8 + 3 * kQ + 20 * kQ + 8;
 
-__host__ __device__ inline size_t tok_smem_bytes(const TokGeom& T, int hpg) {
-  return 1024 + T.offF + (size_t)kFloats * 4 + 16 * 8 + 16 + (size_t)hpg * 4 + 16;
+__host__ __device__ inline size_t tok_smem_bytes(const TokGeom& T) {
+  return 1024 + T.offF + (size_t)kFloats * 4 + 16 * 8 + 16;
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -104,6 +112,25 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ void named_sync_compute() {
   asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
 }
+
+// One work unit: chunk c (tokens t0 .. t0 + len - 1) of batch row bi, group g
+// (the launcher keeps the unit count below 2^31).
+struct TokUnit {
+  int c, g, bi, t0, len;
+};
+__device__ __forceinline__ TokUnit tok_unit(const Plan& p, uint32_t u) {
+  TokUnit w;
+  const uint32_t nc = (uint32_t)p.nc, G = (uint32_t)p.G;
+  const uint32_t r = u / nc, bi = r / G;
+  w.c = (int)(u - r * nc);
+  w.g = (int)(r - bi * G);
+  w.bi = (int)bi;
+  w.t0 = w.c * kQ;
+  w.len = min(kQ, p.L - w.t0);
+  return w;
+}
+// Unit table entry (ints): c, g, bi, t0, len, segment id entering the unit.
+enum { kUc = 0, kUg, kUbi, kUt0, kUlen, kUsin };
 
 __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs f,
                                                                  const __grid_constant__ CUtensorMap tmX,
@@ -125,8 +152,9 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
   uint8_t* sH = sm + T.offH;
   float* lq = reinterpret_cast<float*>(sm + T.offF);  // [3][Q]
   float* dtq = lq + 3 * kQ;                           // [3][Q]
-  int* sq = reinterpret_cast<int*>(dtq + 3 * kQ);     // [Q]
-  float* sfac = reinterpret_cast<float*>(sq + kQ);    // [3][Q] exp(l_{32 rb} - l_j) dt_j, rb = 1..3
+  int* sqr = reinterpret_cast<int*>(dtq + 3 * kQ);    // [kRingU][Q] segment ids
+  int* utab = sqr + kRingU * kQ;                      // [kRingU][8] unit table
+  float* sfac = reinterpret_cast<float*>(utab + kRingU * 8);  // [3][Q] exp(l_{32 rb} - l_j) dt_j, rb = 1..3
   float* pZX = sfac + 3 * kQ;                         // [4 warpgroups][Q] x . Z
   float* pWY = pZX + 4 * kQ;                          // dy . W
   float* pDU = pWY + 4 * kQ;                          // x . dXs
@@ -135,49 +163,50 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
   float* red = pYX + 4 * kQ;                          // [8]
   uint64_t* bar = reinterpret_cast<uint64_t*>(red + 8);
   uint64_t *b_bc = bar, *b_xy = bar + 1, *b_sh = bar + 3, *b_cb = bar + 4, *b_b1 = bar + 5, *b_mr = bar + 6,
-           *b_b2 = bar + 7, *b_ed = bar + 9;
+           *b_b2 = bar + 7, *b_ed = bar + 9, *b_bf = bar + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 16);
-  float* sD = reinterpret_cast<float*>(tmem_slot + 4);  // [hpg]
 
-  const int c = blockIdx.x, g = blockIdx.y, bi = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int wg = (tid >> 7) & 3, r = tid & 127, wq = (tid >> 5) & 3;
   const int wlane = wq * 32;
-  const int t0 = c * kQ, len = min(kQ, p.L - t0);
-  const int hpg = p.hpg, h_first = g * hpg;
-  const long long bh0 = (long long)bi * p.H + h_first;
+  const int hpg = p.hpg;
+  const uint32_t nunits_all = (uint32_t)p.nc * (uint32_t)p.G * (uint32_t)p.b;
+  const int nunits = (int)((nunits_all - blockIdx.x + gridDim.x - 1) / gridDim.x);
+  const int nh = nunits * hpg;  // heads this CTA walks, unit by unit
+  auto unit_of = [&](int i) { return tok_unit(p, blockIdx.x + (uint32_t)i * gridDim.x); };
   const uint32_t c_bytes = (uint32_t)T.ncb * T.cblk;
   const uint32_t s_bytes = (uint32_t)p.N * 128u;
-  auto issue_xy = [&](int hh) {
-    const int buf = hh & 1, h = h_first + hh;
-    mbar_expect_tx(&b_xy[buf], 2 * kTok);
-    tma_load_4d(sXb + buf * kTok, &tmX, &b_xy[buf], 0, h, t0, bi);
-    tma_load_4d(sYb + buf * kTok, &tmY, &b_xy[buf], 0, h, t0, bi);
-  };
-  auto issue_sh = [&](int hh) {
-    const int h = h_first + hh;
-    mbar_expect_tx(b_sh, 2 * s_bytes);
-    tma_load_4d(sS, &tmS, b_sh, 0, 0, c, bi * p.H + h);
-    tma_load_4d(sH, &tmH, b_sh, 0, 0, c, bi * p.H + h);
-  };
-  if (tid == kCompute) {  // control A starts the tile copies first
-    for (int k = 0; k < 10; ++k) mbar_init(&bar[k], 1);  // bc, xy[2], sh, cb, b1, mr, b2[2], ed
-    mbar_fence_init();
-    mbar_expect_tx(b_bc, 2 * c_bytes);
-    for (int q = 0; q < T.ncb; ++q) {
-      tma_load_4d(sB + q * T.cblk, &tmB, b_bc, q * 64, g, t0, bi);
-      tma_load_4d(sC + q * T.cblk, &tmC, b_bc, q * 64, g, t0, bi);
+  // segment ids and table entry of unit i into ring slot i % kRingU
+  // (threads 0 .. Q-1)
+  auto fill_unit = [&](int i) {
+    if (tid < kQ && i < nunits) {
+      const TokUnit w = unit_of(i);
+      const int slot = i % kRingU;
+      sqr[slot * kQ + tid] = tid < w.len ? seg_of(p, f, w.bi, (long long)w.t0 + tid) : -1;
+      if (tid == 0) {
+        int* u = utab + slot * 8;
+        u[kUc] = w.c;
+        u[kUg] = w.g;
+        u[kUbi] = w.bi;
+        u[kUt0] = w.t0;
+        u[kUlen] = w.len;
+        u[kUsin] = seg_in_of(p, f, w.bi, w.c);
+      }
     }
-    issue_xy(0);
-    if (hpg > 1) issue_xy(1);
-    issue_sh(0);
+  };
+  if (tid == kCompute) {
+    for (int k = 0; k < 11; ++k) mbar_init(&bar[k], 1);  // bc, xy[2], sh, cb, b1, mr, b2[2], ed[2]
+    mbar_init(b_bf, kCompute / 32);                      // one arrival per compute warp
+    mbar_fence_init();
   }
-  for (int t = tid; t < kQ; t += kThr) sq[t] = t < len ? seg_of(p, f, bi, (long long)t0 + t) : -1;
-  if (tid < kQ) {  // scalars of the group's first head into slot 0
-    lq[tid] = f.lcs[bh0 * p.Lp + t0 + tid];
-    dtq[tid] = f.dte[bh0 * p.Lp + t0 + tid];
+  fill_unit(0);
+  fill_unit(1);
+  if (tid < kQ && nh > 0) {  // scalars of the first head into slot 0
+    const TokUnit w = unit_of(0);
+    const long long bh = (long long)w.bi * p.H + w.g * hpg;
+    lq[tid] = f.lcs[bh * p.Lp + w.t0 + tid];
+    dtq[tid] = f.dte[bh * p.Lp + w.t0 + tid];
   }
-  for (int k = tid; k < hpg; k += kThr) sD[k] = f.D[h_first + k];
   if (warp == 0) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
@@ -192,272 +221,376 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
 
   if (warp >= kCompute / 32) {
     const int cw = warp - kCompute / 32;
-    if (lane == 0) {
+    if (lane == 0 && nh > 0) {
       const uint32_t id128 = idesc_bf16(128, 128, 0, 0), id64 = idesc_bf16(128, 64, 0, 1);
       const uint32_t id64t = idesc_bf16(128, 64, 1, 1);
+      // row width of the B/C tile is 32, 64 or 128 bytes: shifts, not divisions
+      const uint32_t lcw = T.cw == 128 ? 7u : (T.cw == 64 ? 6u : 5u);
       auto kdesc_c = [&](const uint8_t* t, int ks) {  // K-major B/C tile, K = d_state
-        const uint32_t kb = (ks * 32) / T.cw, kin = (ks * 32) % T.cw;
+        const uint32_t kb = ((uint32_t)ks * 32u) >> lcw, kin = ((uint32_t)ks * 32u) & (T.cw - 1u);
         return smem_desc(smem_u32(t) + kb * T.cblk + kin, 16, 8 * T.cw, T.cswz);
       };
       auto mndesc_rows = [&](const uint8_t* t, int ks) {  // MN-major (64 wide), K along rows
         return smem_desc(smem_u32(t) + ks * 16 * 128, 16, 1024, kSwz128);
       };
+      // copies of head hh of unit w into buffer buf, and its dx store
+      auto issue_xy = [&](const TokUnit& w, int hh, int buf) {
+        const int h = w.g * hpg + hh;
+        mbar_expect_tx(&b_xy[buf], 2 * kTok);
+        tma_load_4d(sXb + buf * kTok, &tmX, &b_xy[buf], 0, h, w.t0, w.bi);
+        tma_load_4d(sYb + buf * kTok, &tmY, &b_xy[buf], 0, h, w.t0, w.bi);
+      };
+      auto store_dx = [&](const TokUnit& w, int hh, int buf) {
+        tma_store_4d(&tmDX, sYb + buf * kTok, 0, w.g * hpg + hh, w.t0, w.bi);
+        bulk_commit();
+      };
+      TokUnit uprev, ucur = unit_of(0), unext = unit_of(nunits > 1 ? 1 : 0);
+      uprev = ucur;
       if (cw == 0) {
-        // ---------------- control A: copies, C B^T, per head dXs and Yc ----------------
-        wait(b_bc, 0);
-        tc_fence_after();
-        for (int ks = 0; ks < p.N / 16; ++ks)  // C B^T (M = i, N = j, K = d_state), once per group
-          mma_bf16(tCB, kdesc_c(sC, ks), kdesc_c(sB, ks), id128, ks > 0);
-        mma_commit(b_cb);
-        for (int hh = 0; hh < hpg; ++hh) {
-          wait(b_sh, hh & 1);
-          if (hh >= 1) {
-            // the epilogue of head hh-1 has read dXs, Yc and its x, dy buffer
-            // and left that head's dx in the dy tile: store it, then refill
-            // the buffer once the store has read it
-            wait(b_ed, (hh - 1) & 1);
-            tma_store_4d(&tmDX, sYb + ((hh - 1) & 1) * kTok, 0, h_first + hh - 1, t0, bi);
-            bulk_commit();
-            if (hh + 1 < hpg) {
-              bulk_wait_read<0>();
-              issue_xy(hh + 1);
-            }
+        // ---------------- control A: B, C, dS, H copies; C B^T; per head dXs and Yc ----------------
+        auto issue_sh = [&](const TokUnit& w, int hh) {
+          const int bhh = w.bi * p.H + w.g * hpg + hh;
+          mbar_expect_tx(b_sh, 2 * s_bytes);
+          tma_load_4d(sS, &tmS, b_sh, 0, 0, w.c, bhh);
+          tma_load_4d(sH, &tmH, b_sh, 0, 0, w.c, bhh);
+        };
+        auto issue_bc = [&](const TokUnit& w) {
+          mbar_expect_tx(b_bc, 2 * c_bytes);
+          for (int q = 0; q < T.ncb; ++q) {
+            tma_load_4d(sB + q * T.cblk, &tmB, b_bc, q * 64, w.g, w.t0, w.bi);
+            tma_load_4d(sC + q * T.cblk, &tmC, b_bc, q * 64, w.g, w.t0, w.bi);
           }
+        };
+        issue_bc(ucur);
+        issue_sh(ucur, 0);
+        int i = 0, hh = 0;  // unit and head of k
+        for (int k = 0; k < nh; ++k) {
+          if (hh == 0) {
+            if (k > 0) {
+              ucur = unext;
+              unext = unit_of(i + 1 < nunits ? i + 1 : i);
+            }
+            wait(b_bc, i & 1);
+            // the mask pass of the previous unit's last head has read C B^T
+            if (k > 0) wait(b_mr, (k - 1) & 1);
+            tc_fence_after();
+            for (int ks = 0; ks < p.N / 16; ++ks)  // C B^T (M = i, N = j, K = d_state), once per unit
+              mma_bf16(tCB, kdesc_c(sC, ks), kdesc_c(sB, ks), id128, ks > 0);
+            mma_commit(b_cb);
+          }
+          wait(b_sh, k & 1);
+          if (k >= 1) wait(b_bf, (k - 1) & 1);  // the previous head's epilogue has read dXs, Yc
           tc_fence_after();
           for (int ks = 0; ks < p.N / 16; ++ks) {
             mma_bf16(tDXS, kdesc_c(sB, ks), mndesc_rows(sS, ks), id64, ks > 0);
             mma_bf16(tYC, kdesc_c(sC, ks), mndesc_rows(sH, ks), id64, ks > 0);
           }
           mma_commit(b_b1);
-          if (hh + 1 < hpg) {
-            wait(b_b1, hh & 1);  // dS, H read
-            issue_sh(hh + 1);
+          if (k + 1 < nh) {
+            wait(b_b1, k & 1);  // dS, H read; the unit's B, C too if this was its last head
+            if (hh + 1 == hpg) {
+              issue_bc(unext);
+              issue_sh(unext, 0);
+            } else {
+              issue_sh(ucur, hh + 1);
+            }
+          }
+          if (++hh == hpg) {
+            hh = 0;
+            ++i;
           }
         }
-        wait(b_ed, (hpg - 1) & 1);  // the last head's dx
-        tma_store_4d(&tmDX, sYb + ((hpg - 1) & 1) * kTok, 0, h_first + hpg - 1, t0, bi);
-        bulk_commit();
-        bulk_wait_all();
       } else {
-        // ---------------- control B: per head Z = M^T dY, W = M X ----------------
-        for (int hh = 0; hh < hpg; ++hh) {
-          // M of head hh written; the pair hh & 1 was read by the epilogue
-          // of head hh-2, which the compute warps finished first; x, dy of
-          // head hh landed (the mask pass does not read them)
-          wait(b_mr, hh & 1);
-          wait(&b_xy[hh & 1], (hh >> 1) & 1);
+        // ---------------- control B: x, dy copies; per head Z = M^T dY, W = M X; dx stores ----------------
+        issue_xy(ucur, 0, 0);
+        if (nh > 1) {
+          if (hpg > 1) issue_xy(ucur, 1, 1);
+          else issue_xy(unext, 0, 1);
+        }
+        int i = 0, hh = 0;  // unit and head of k
+        for (int k = 0; k < nh; ++k) {
+          if (hh == 0 && k > 0) {
+            uprev = ucur;
+            ucur = unext;
+            unext = unit_of(i + 1 < nunits ? i + 1 : i);
+          }
+          // M of head k written; the pair k & 1 was read by the epilogue of
+          // head k-2, which the compute warps finished first; x, dy of head
+          // k landed (the mask pass does not read them)
+          wait(b_mr, k & 1);
+          wait(&b_xy[k & 1], (k >> 1) & 1);
           tc_fence_after();
-          const uint32_t tz = tZW + (hh & 1) * 128, tw = tz + 64;
-          const uint8_t* sY = sYb + (hh & 1) * kTok;
-          const uint8_t* sX = sXb + (hh & 1) * kTok;
+          const uint32_t tz = tZW + (k & 1) * 128, tw = tz + 64;
+          const uint8_t* sY = sYb + (k & 1) * kTok;
+          const uint8_t* sX = sXb + (k & 1) * kTok;
           for (int ks = 0; ks < kQ / 16; ++ks) {
             const uint64_t am = smem_desc(smem_u32(sA) + ks * 16 * 128, kTok, 1024, kSwz128);   // M^T
             const uint64_t ak = smem_desc(smem_u32(sA) + (ks / 4) * kTok + (ks % 4) * 32, 16, 1024, kSwz128);
             mma_bf16(tz, am, mndesc_rows(sY, ks), id64t, ks > 0);
             mma_bf16(tw, ak, mndesc_rows(sX, ks), id64, ks > 0);
           }
-          mma_commit(&b_b2[hh & 1]);
+          mma_commit(&b_b2[k & 1]);
+          if (k >= 1) {
+            // the previous head's epilogue left its dx in its dy tile: store
+            // it, then refill that buffer with the next head once the store
+            // has read it
+            wait(&b_ed[(k - 1) & 1], ((k - 1) >> 1) & 1);
+            if (hh == 0) store_dx(uprev, hpg - 1, (k - 1) & 1);
+            else store_dx(ucur, hh - 1, (k - 1) & 1);
+            if (k + 1 < nh) {
+              bulk_wait_read<0>();
+              if (hh + 1 == hpg) issue_xy(unext, 0, (k + 1) & 1);
+              else issue_xy(ucur, hh + 1, (k + 1) & 1);
+            }
+          }
+          if (++hh == hpg) {
+            hh = 0;
+            ++i;
+          }
         }
+        wait(&b_ed[(nh - 1) & 1], ((nh - 1) >> 1) & 1);  // the last head's dx
+        store_dx(ucur, hpg - 1, (nh - 1) & 1);
+        bulk_wait_all();
       }
     }
-  } else {
+  } else if (nh > 0) {
     // ---------------- 16 compute warps ----------------
-    const int s_in = seg_in_of(p, f, bi, c);
-    const int s_last = sq[len - 1];
-    const bool one_seg = sq[0] == s_last;  // seq_idx is nondecreasing: no reset inside the chunk
-    const int i = wlane + lane;            // row of this thread in the mask pass
-    const bool tok_ok = i < len;
-    const int si = tok_ok ? sq[i] : -2;
-    const int lim = tok_ok ? i : -1;
-    // per-head factor table exp(l_{32 rb} - l_j) (j < 32 rb), from slot `slot`
-    auto fill_fac = [&](int slot) {
+    const int i_row = wlane + lane;  // row of this thread in the mask pass
+    // per-head factor table exp(l_{32 rb} - l_j) dt_j (j < 32 rb) of head k of unit iu
+    auto fill_fac = [&](int k, int iu) {
       if (tid < 3 * kQ) {
-        const int rb = 1 + tid / kQ, j = tid % kQ;
+        const int slot = k % 3, rb = 1 + tid / kQ, j = tid % kQ;
+        const int len = utab[(iu % kRingU) * 8 + kUlen];
         const float* lb = lq + slot * kQ;
         const float* db = dtq + slot * kQ;
         sfac[tid] = (j < 32 * rb && j < len) ? __expf(lb[32 * rb] - lb[j]) * db[j] : 0.0f;
       }
     };
-    fill_fac(0);
+    fill_fac(0, 0);
     // upper-triangle 16-column units of the M tile: zero once
     for (int q = 2 * wq + 2 + wg; q < 8; q += 4) {
       uint8_t* blk = sA + (q >> 2) * kTok;
       const uint32_t e0 = (q & 3) * 16;
-      *reinterpret_cast<uint4*>(blk + swz128_off(i, e0)) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(blk + swz128_off(i, e0 + 8)) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(blk + swz128_off(i_row, e0)) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(blk + swz128_off(i_row, e0 + 8)) = make_uint4(0, 0, 0, 0);
     }
     named_sync_compute();
-    wait(b_cb, 0);
-    tc_fence_after();
-    for (int hh = 0; hh <= hpg; ++hh) {
-      if (hh < hpg) {
-        const int slot = hh % 3;
-        const float* lb = lq + slot * kQ;
-        const float* db = dtq + slot * kQ;
-        if (hh + 1 < hpg && tid < kQ) {  // scalars of head hh+1 (slot last read by head hh-2)
-          const int sn = (hh + 1) % 3;
-          cp_async4(lq + sn * kQ + tid, f.lcs + (bh0 + hh + 1) * p.Lp + t0 + tid);
-          cp_async4(dtq + sn * kQ + tid, f.dte + (bh0 + hh + 1) * p.Lp + t0 + tid);
-        }
-        cp_async_commit();
-        if (hh >= 1) {  // Z, W of head hh-1 done: M may be rewritten
-          wait(&b_b2[(hh - 1) & 1], ((hh - 1) >> 1) & 1);
-          tc_fence_after();
-        }
-        // ---- M tile: row i, 16-column units of this row block
-        const bool fact = one_seg && f.A[h_first + hh] <= 0.0f;
-        const float li = tok_ok ? lb[i] : lb[len - 1];
-        const float r_row = wq > 0 ? __expf(li - lb[32 * wq]) : 0.0f;
-        for (int q = wg; q <= 2 * wq + 1; q += 4) {
-          const int j0 = q * 16;
-          uint32_t pk[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-          if (j0 < len) {  // warp-uniform
-            float v[16];
-            tmem_ld16(tmem_addr(tCB, wlane, j0), v);
-            if (fact && q < 2 * wq) {
-              const float* s = sfac + (wq - 1) * kQ;
+
+    // ---- M tile of head k (head hh of unit iu); then the factor table of head k+1
+    auto mask_pass = [&](int k, int iu, int hh) {
+      const int us = iu % kRingU;
+      const int* ut = utab + us * 8;
+      const int* sq = sqr + us * kQ;
+      const int slot = k % 3;
+      const float* lb = lq + slot * kQ;
+      const float* db = dtq + slot * kQ;
+      if (hh == 0) {
+        // table entries of the unit after next: its ring slot was last read by
+        // the epilogues of the unit two back, all done
+        fill_unit(iu + 2);
+        wait(b_cb, iu & 1);
+        tc_fence_after();
+      }
+      const int iu_n = hh + 1 == hpg ? iu + 1 : iu, hh_n = hh + 1 == hpg ? 0 : hh + 1;
+      if (k + 1 < nh && tid < kQ) {  // scalars of head k+1 (slot last read by head k-2)
+        const int* un = utab + (iu_n % kRingU) * 8;
+        const long long bhn = (long long)un[kUbi] * p.H + un[kUg] * hpg + hh_n;
+        const int sn = (k + 1) % 3;
+        cp_async4(lq + sn * kQ + tid, f.lcs + bhn * p.Lp + un[kUt0] + tid);
+        cp_async4(dtq + sn * kQ + tid, f.dte + bhn * p.Lp + un[kUt0] + tid);
+      }
+      cp_async_commit();
+      if (k >= 1) {  // Z, W of head k-1 done: M may be rewritten
+        wait(&b_b2[(k - 1) & 1], ((k - 1) >> 1) & 1);
+        tc_fence_after();
+      }
+      const int len = ut[kUlen];
+      const int s_last = sq[len - 1];
+      const bool one_seg = sq[0] == s_last;  // seq_idx is nondecreasing: no reset inside the chunk
+      const bool tok_ok = i_row < len;
+      const int si = tok_ok ? sq[i_row] : -2;
+      const int lim = tok_ok ? i_row : -1;
+      const bool fact = one_seg && f.A[ut[kUg] * hpg + hh] <= 0.0f;
+      const float li = tok_ok ? lb[i_row] : lb[len - 1];
+      const float r_row = wq > 0 ? __expf(li - lb[32 * wq]) : 0.0f;
+      for (int q = wg; q <= 2 * wq + 1; q += 4) {
+        const int j0 = q * 16;
+        uint32_t pk[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (j0 < len) {  // warp-uniform
+          float v[16];
+          tmem_ld16(tmem_addr(tCB, wlane, j0), v);
+          if (fact && q < 2 * wq) {
+            const float* s = sfac + (wq - 1) * kQ;
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float4 sj = *reinterpret_cast<const float4*>(s + j0 + 4 * k);
-                pk[2 * k] = pack2(v[4 * k] * sj.x * r_row, v[4 * k + 1] * sj.y * r_row);
-                pk[2 * k + 1] = pack2(v[4 * k + 2] * sj.z * r_row, v[4 * k + 3] * sj.w * r_row);
+            for (int kk = 0; kk < 4; ++kk) {
+              const float4 sj = *reinterpret_cast<const float4*>(s + j0 + 4 * kk);
+              pk[2 * kk] = pack2(v[4 * kk] * sj.x * r_row, v[4 * kk + 1] * sj.y * r_row);
+              pk[2 * kk + 1] = pack2(v[4 * kk + 2] * sj.z * r_row, v[4 * kk + 3] * sj.w * r_row);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const float4 lj = *reinterpret_cast<const float4*>(lb + j0 + 4 * kk);
+              const float4 dj = *reinterpret_cast<const float4*>(db + j0 + 4 * kk);
+              int4 sj = make_int4(si, si, si, si);
+              if (!one_seg) sj = *reinterpret_cast<const int4*>(sq + j0 + 4 * kk);
+              const float lv[4] = {lj.x, lj.y, lj.z, lj.w}, dv[4] = {dj.x, dj.y, dj.z, dj.w};
+              const int sv[4] = {sj.x, sj.y, sj.z, sj.w};
+              float a[4];
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const bool on = j0 + 4 * kk + m <= lim && sv[m] == si;
+                a[m] = v[4 * kk + m] * __expf(on ? li - lv[m] : -INFINITY) * dv[m];
               }
-            } else {
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float4 lj = *reinterpret_cast<const float4*>(lb + j0 + 4 * k);
-                const float4 dj = *reinterpret_cast<const float4*>(db + j0 + 4 * k);
-                int4 sj = make_int4(si, si, si, si);
-                if (!one_seg) sj = *reinterpret_cast<const int4*>(sq + j0 + 4 * k);
-                const float lv[4] = {lj.x, lj.y, lj.z, lj.w}, dv[4] = {dj.x, dj.y, dj.z, dj.w};
-                const int sv[4] = {sj.x, sj.y, sj.z, sj.w};
-                float a[4];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                  const bool on = j0 + 4 * k + m <= lim && sv[m] == si;
-                  a[m] = v[4 * k + m] * __expf(on ? li - lv[m] : -INFINITY) * dv[m];
-                }
-                pk[2 * k] = pack2(a[0], a[1]);
-                pk[2 * k + 1] = pack2(a[2], a[3]);
-              }
+              pk[2 * kk] = pack2(a[0], a[1]);
+              pk[2 * kk + 1] = pack2(a[2], a[3]);
             }
           }
-          uint8_t* blk = sA + (q >> 2) * kTok;
-          const uint32_t e0 = (q & 3) * 16;
-          *reinterpret_cast<uint4*>(blk + swz128_off(i, e0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(blk + swz128_off(i, e0 + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
-        cp_async_wait_all();  // scalars of head hh+1 landed (visible after the barrier)
-        fence_async_smem();
-        tc_fence_before();
-        named_sync_compute();  // M complete; C B^T reads of this head done
-        if (tid == 0) mbar_arrive(b_mr);
-        // factor table of the next head: its scalars are visible since the
-        // barrier, and this head's mask pass is done with the table; the
-        // epilogue's barriers (or the one below) order it before that head's
-        // mask pass
-        if (hh + 1 < hpg) fill_fac((hh + 1) % 3);
-        if (hh == 0) named_sync_compute();
+        uint8_t* blk = sA + (q >> 2) * kTok;
+        const uint32_t e0 = (q & 3) * 16;
+        *reinterpret_cast<uint4*>(blk + swz128_off(i_row, e0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(blk + swz128_off(i_row, e0 + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
-      if (hh >= 1) {
-        // ---- epilogue of head e = hh - 1: token t = r, headdim columns 16 wg ..
-        const int e = hh - 1, slot = e % 3, buf = e & 1, h = h_first + e;
-        const long long bh = bh0 + e;
-        const float* lb = lq + slot * kQ;
-        const float* db = dtq + slot * kQ;
-        const int t = r;
-        const bool tv = t < len;
-        wait(b_b1, e & 1);
-        wait(&b_xy[buf], (e >> 1) & 1);
-        if (hh == hpg) wait(&b_b2[buf], (e >> 1) & 1);
-        tc_fence_after();
-        const uint8_t* sX = sXb + buf * kTok;
-        const uint8_t* sY = sYb + buf * kTok;
-        const uint32_t tz = tZW + buf * 128, tw = tz + 64;
-        // the accumulator rows in two halves (Z, dXs for dx; then W, Yc), so that
-        // no more than 32 of them are live at once; the first half's reads are
-        // in flight while the x, dy rows come from shared memory
-        uint32_t zr[16], sr[16];
-        tmem_ld16_issue(tmem_addr(tz, wlane, wg * 16), zr);
-        tmem_ld16_issue(tmem_addr(tDXS, wlane, wg * 16), sr);
-        uint4* y0p = reinterpret_cast<uint4*>(const_cast<uint8_t*>(sY) + swz128_off(t, wg * 16));
-        uint4* y1p = reinterpret_cast<uint4*>(const_cast<uint8_t*>(sY) + swz128_off(t, wg * 16 + 8));
-        const uint4 x0 = *reinterpret_cast<const uint4*>(sX + swz128_off(t, wg * 16));
-        const uint4 x1 = *reinterpret_cast<const uint4*>(sX + swz128_off(t, wg * 16 + 8));
-        const uint4 y0 = *y0p;
-        const uint4 y1 = *y1p;
-        tmem_ld_wait2(zr, sr);
-        float z[16], s16[16];
+      cp_async_wait_all();  // scalars of head k+1 landed (visible after the barrier)
+      fence_async_smem();
+      tc_fence_before();
+      named_sync_compute();  // M complete; C B^T reads of this head done
+      if (tid == 0) mbar_arrive(b_mr);
+      // factor table of the next head: its scalars are visible since the
+      // barrier, and this head's mask pass is done with the table; a later
+      // barrier orders it before that head's mask pass
+      if (k + 1 < nh) fill_fac(k + 1, iu_n);
+    };
+
+    // ---- epilogue of head e (head eh of unit eu): token t = r, headdim columns 16 wg ..
+    auto epilogue = [&](int e, int eu, int eh) {
+      const int us = eu % kRingU;
+      const int* ut = utab + us * 8;
+      const int* sq = sqr + us * kQ;
+      const int slot = e % 3, buf = e & 1;
+      const int h = ut[kUg] * hpg + eh, c = ut[kUc], t0 = ut[kUt0], len = ut[kUlen], bi = ut[kUbi];
+      const long long bh = (long long)bi * p.H + h;
+      const int s_last = sq[len - 1], s_in = ut[kUsin];
+      const float* lb = lq + slot * kQ;
+      const float* db = dtq + slot * kQ;
+      const int t = r;
+      const bool tv = t < len;
+      const float Dh = __ldg(f.D + h);
+      wait(b_b1, e & 1);
+      wait(&b_xy[buf], (e >> 1) & 1);
+      wait(&b_b2[buf], (e >> 1) & 1);
+      tc_fence_after();
+      const uint8_t* sX = sXb + buf * kTok;
+      const uint8_t* sY = sYb + buf * kTok;
+      const uint32_t tz = tZW + buf * 128, tw = tz + 64;
+      // the accumulator rows in two halves (Z, dXs for dx; then W, Yc), so that
+      // no more than 32 of them are live at once; the first half's reads are
+      // in flight while the x, dy rows come from shared memory
+      uint32_t zr[16], sr[16];
+      tmem_ld16_issue(tmem_addr(tz, wlane, wg * 16), zr);
+      tmem_ld16_issue(tmem_addr(tDXS, wlane, wg * 16), sr);
+      uint4* y0p = reinterpret_cast<uint4*>(const_cast<uint8_t*>(sY) + swz128_off(t, wg * 16));
+      uint4* y1p = reinterpret_cast<uint4*>(const_cast<uint8_t*>(sY) + swz128_off(t, wg * 16 + 8));
+      const uint4 x0 = *reinterpret_cast<const uint4*>(sX + swz128_off(t, wg * 16));
+      const uint4 x1 = *reinterpret_cast<const uint4*>(sX + swz128_off(t, wg * 16 + 8));
+      const uint4 y0 = *y0p;
+      const uint4 y1 = *y1p;
+      tmem_ld_wait2(zr, sr);
+      float z[16], s16[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          z[k] = __uint_as_float(zr[k]);
-          s16[k] = __uint_as_float(sr[k]);
-        }
-        const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        const uint32_t ys[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-        const float dtt = tv ? db[t] : 0.0f;
-        const float lt = tv ? lb[t] : 0.0f;
-        const float wt = (tv && sq[t] == s_last) ? __expf(lb[len - 1] - lt) : 0.0f;
-        const float ut = wt * dtt;
-        const float Dh = sD[e];
-        float zx = 0.0f, wy = 0.0f, du = 0.0f, ca = 0.0f, yx = 0.0f;
-        uint32_t o[8];
+      for (int kk = 0; kk < 16; ++kk) {
+        z[kk] = __uint_as_float(zr[kk]);
+        s16[kk] = __uint_as_float(sr[kk]);
+      }
+      const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const uint32_t ys[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+      const float dtt = tv ? db[t] : 0.0f;
+      const float lt = tv ? lb[t] : 0.0f;
+      const float wt = (tv && sq[t] == s_last) ? __expf(lb[len - 1] - lt) : 0.0f;
+      const float ut_ = wt * dtt;
+      float zx = 0.0f, wy = 0.0f, du = 0.0f, ca = 0.0f, yx = 0.0f;
+      uint32_t o[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float2 xv = unpack2(xs[k]), yv = unpack2(ys[k]);
-          zx = fmaf(xv.x, z[2 * k], fmaf(xv.y, z[2 * k + 1], zx));
-          du = fmaf(xv.x, s16[2 * k], fmaf(xv.y, s16[2 * k + 1], du));
-          yx = fmaf(yv.x, xv.x, fmaf(yv.y, xv.y, yx));
-          o[k] = pack2(z[2 * k] + fmaf(ut, s16[2 * k], Dh * yv.x),
-                       z[2 * k + 1] + fmaf(ut, s16[2 * k + 1], Dh * yv.y));
-        }
-        {
-          float w16[16], y16[16];
-          tmem_ld16x2(tmem_addr(tw, wlane, wg * 16), tmem_addr(tYC, wlane, wg * 16), w16, y16);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float2 yv = unpack2(ys[k]);
-            wy = fmaf(yv.x, w16[2 * k], fmaf(yv.y, w16[2 * k + 1], wy));
-            ca = fmaf(yv.x, y16[2 * k], fmaf(yv.y, y16[2 * k + 1], ca));
-          }
-        }
-        // dx in place of this thread's dy row piece (already read), for the
-        // tensor store of the whole tile (rows past the sequence are clipped)
-        *y0p = make_uint4(o[0], o[1], o[2], o[3]);
-        *y1p = make_uint4(o[4], o[5], o[6], o[7]);
-        pZX[wg * kQ + t] = zx;
-        pWY[wg * kQ + t] = wy;
-        pDU[wg * kQ + t] = du;
-        pCA[wg * kQ + t] = ca;
-        pYX[wg * kQ + t] = tv ? yx : 0.0f;
+      for (int kk = 0; kk < 8; ++kk) {
+        const float2 xv = unpack2(xs[kk]), yv = unpack2(ys[kk]);
+        zx = fmaf(xv.x, z[2 * kk], fmaf(xv.y, z[2 * kk + 1], zx));
+        du = fmaf(xv.x, s16[2 * kk], fmaf(xv.y, s16[2 * kk + 1], du));
+        yx = fmaf(yv.x, xv.x, fmaf(yv.y, xv.y, yx));
+        o[kk] = pack2(z[2 * kk] + fmaf(ut_, s16[2 * kk], Dh * yv.x),
+                      z[2 * kk + 1] + fmaf(ut_, s16[2 * kk + 1], Dh * yv.y));
+      }
+      {
+        float w16[16], y16[16];
+        tmem_ld16x2(tmem_addr(tw, wlane, wg * 16), tmem_addr(tYC, wlane, wg * 16), w16, y16);
+        // dXs and Yc of this head are read: the next head's may be formed
         tc_fence_before();
-        fence_async_smem();  // x and dy are next written by tensor copies (async proxy)
-        named_sync_compute();  // TMEM pair, dXs, Yc, x, dy read back; partials complete
-        if (tid == 0) mbar_arrive(b_ed);
-        if (wg == 0) {
-          auto fold = [&](const float* a) { return (a[t] + a[kQ + t]) + (a[2 * kQ + t] + a[3 * kQ + t]); };
-          const float colr = fold(pZX), roww = fold(pWY), dut = fold(pDU), car = fold(pCA);
-          float udu = 0.0f;
-          if (tv) {
-            const float cv = sq[t] == s_in ? __expf(lt) : 0.0f;
-            const float colq = dtt > 1e-30f ? colr / dtt : 0.0f;
-            const float dd = colq + wt * dut;
-            const float dl = roww - colr + cv * car - ut * dut;
-            f.ddte[bh * p.Lp + t0 + t] = dd;
-            f.dl[bh * p.Lp + t0 + t] = dl;
-            udu = ut * dut;
-          }
-          // per-chunk sums: one slot per warp (row block), added in slot
-          // order by the parameter-gradient kernels
-          udu = warp_sum(udu);
-          if (lane == 0) f.udu[(bh * p.nc + c) * p.cb_ntb + wq] = udu;
-        } else if (wg == 1) {
-          float v = (pYX[t] + pYX[kQ + t]) + (pYX[2 * kQ + t] + pYX[3 * kQ + t]);
-          v = warp_sum(v);
-          if (lane == 0) f.pdD[(((long long)bi * p.nc + c) * p.cb_ntb + wq) * p.H + h] = v;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_bf);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const float2 yv = unpack2(ys[kk]);
+          wy = fmaf(yv.x, w16[2 * kk], fmaf(yv.y, w16[2 * kk + 1], wy));
+          ca = fmaf(yv.x, y16[2 * kk], fmaf(yv.y, y16[2 * kk + 1], ca));
         }
-        // the partial arrays are next written after the next barrier, which
-        // these readers pass only after reading them
+      }
+      // dx in place of this thread's dy row piece (already read), for the
+      // tensor store of the whole tile (rows past the sequence are clipped)
+      *y0p = make_uint4(o[0], o[1], o[2], o[3]);
+      *y1p = make_uint4(o[4], o[5], o[6], o[7]);
+      pZX[wg * kQ + t] = zx;
+      pWY[wg * kQ + t] = wy;
+      pDU[wg * kQ + t] = du;
+      pCA[wg * kQ + t] = ca;
+      pYX[wg * kQ + t] = tv ? yx : 0.0f;
+      tc_fence_before();
+      fence_async_smem();  // x and dy are next written by tensor copies (async proxy)
+      named_sync_compute();  // TMEM pair, x, dy read back; partials complete
+      if (tid == 0) mbar_arrive(&b_ed[e & 1]);
+      if (wg == 0) {
+        auto fold = [&](const float* a) { return (a[t] + a[kQ + t]) + (a[2 * kQ + t] + a[3 * kQ + t]); };
+        const float colr = fold(pZX), roww = fold(pWY), dut = fold(pDU), car = fold(pCA);
+        float udu = 0.0f;
+        if (tv) {
+          const float cv = sq[t] == s_in ? __expf(lt) : 0.0f;
+          const float colq = dtt > 1e-30f ? colr / dtt : 0.0f;
+          const float dd = colq + wt * dut;
+          const float dl = roww - colr + cv * car - ut_ * dut;
+          f.ddte[bh * p.Lp + t0 + t] = dd;
+          f.dl[bh * p.Lp + t0 + t] = dl;
+          udu = ut_ * dut;
+        }
+        // per-chunk sums: one slot per warp (row block), added in slot
+        // order by the parameter-gradient kernels
+        udu = warp_sum(udu);
+        if (lane == 0) f.udu[(bh * p.nc + c) * p.cb_ntb + wq] = udu;
+      } else if (wg == 1) {
+        float v = (pYX[t] + pYX[kQ + t]) + (pYX[2 * kQ + t] + pYX[3 * kQ + t]);
+        v = warp_sum(v);
+        if (lane == 0) f.pdD[(((long long)bi * p.nc + c) * p.cb_ntb + wq) * p.H + h] = v;
+      }
+      // the partial arrays are next written after the next barrier, which
+      // these readers pass only after reading them
+    };
+
+    // Per head k: the M tile of k, then the epilogue of k-1 while the tensor
+    // core forms Z, W of k.  At the first head of a unit the epilogue of the
+    // previous unit's last head goes first: it covers the copies of the new
+    // unit's B, C and its C B^T.
+    int iu = 0, hh = 0, eu = 0, eh = 0;  // unit and head of k, of k-1
+    for (int k = 0; k <= nh; ++k) {
+      const bool epi_first = k >= 1 && (k == nh || hh == 0);
+      if (epi_first) epilogue(k - 1, eu, eh);
+      if (k < nh) {
+        mask_pass(k, iu, hh);
+        if (k >= 1 && !epi_first) epilogue(k - 1, eu, eh);
+        else named_sync_compute();  // the factor table before the next mask pass
+      }
+      eu = iu;
+      eh = hh;
+      if (++hh == hpg) {
+        hh = 0;
+        ++iu;
       }
     }
   }
@@ -492,10 +625,16 @@ cudaError_t launch_chunk_bwd_tok_tc(const Plan& p, const Bufs& f, cudaStream_t s
       !encode_tmap_bf16_4d(&S, f.dS, ds, ss, bs, 128) || !encode_tmap_bf16_4d(&H, f.Hin, ds, ss, bs, 128) ||
       !encode_tmap_bf16_4d(&DX, f.dx, dxx, sxx, bxx, 128))
     return cudaErrorInvalidValue;
-  const size_t smem = tok_smem_bytes(T, p.hpg);
+  const size_t smem = tok_smem_bytes(T);
   cudaError_t e = cudaFuncSetAttribute(chunk_bwd_tok_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  chunk_bwd_tok_tc_kernel<<<dim3(p.nc, p.G, p.b), kThr, smem, s>>>(p, f, X, Y, B, C, S, H, DX);
+  // one persistent CTA per SM (one fits: shared memory and all 512 TMEM
+  // columns), at most one per work unit
+  const long long units = (long long)p.nc * p.G * p.b;
+  if (units >= (1ll << 31)) return cudaErrorInvalidValue;
+  const long long sms = device_sm_count();
+  const int grid = (int)(units < sms ? units : sms);
+  chunk_bwd_tok_tc_kernel<<<grid, kThr, smem, s>>>(p, f, X, Y, B, C, S, H, DX);
   return cudaGetLastError();
 }
 
