@@ -54,7 +54,7 @@ def eval_chunk(cfg, dtype_bytes):
     return 128 if tc else cfg["chunk"]
 
 
-def kernel_model(cfg, dtype_bytes):
+def kernel_model(cfg, dtype_bytes, keep=False):
     b, L, H, P, N, G = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate",
                                           "ngroups"))
     Q = eval_chunk(cfg, dtype_bytes)
@@ -110,7 +110,10 @@ def kernel_model(cfg, dtype_bytes):
     # Y2 = C H_in^T, S^T = B^T (w.X) (M = 128 rows issued) and Y1 = A_hat X
     nq = -(-L // 128)
     fq = 2 * 128 * 128 * N + 2 * 128 * P * N + 2 * 128 * P * 128 + 2 * 128 * 128 * P
-    m["ssd_fwd_fused"] = dict(bytes=2 * tokx + T * H * s + 2 * tokbc + 2 * b * H * P * N * 4,
+    # (keeping its intermediates for the backward it also writes the carry-in
+    # states, dt_eff, the chunk cumsums and the per-chunk decays)
+    kept = stS + 2 * per_tok + b * H * nc * 4 if keep else 0
+    m["ssd_fwd_fused"] = dict(bytes=2 * tokx + T * H * s + 2 * tokbc + 2 * b * H * P * N * 4 + kept,
                               flops=b * H * nq * fq)
     m["param_reduce"] = dict(bytes=b * nc * H * 4 * 4, flops=0)
     m["status_reset"] = dict(bytes=4, flops=0)
@@ -380,6 +383,14 @@ def workload_config(name):
     return out
 
 
+def step_flags(args):
+    """Flags of the benchmarked step: its forward keeps the intermediates the
+    backward would recompute, and the backward takes them (the usual
+    training step); --recompute benchmarks the stateless backward."""
+    from mamba_selective_state_gb300 import _lib
+    return 0 if args.recompute else _lib.SSD_KEEP_FWD_STATES
+
+
 # ----------------------------------------------------------------------------
 def run_gpu(args, world, rank, local):
     import torch
@@ -388,7 +399,7 @@ def run_gpu(args, world, rank, local):
     from mamba_selective_state_gb300.runner import SSDDevice
 
     inp = make_workload(args.workload, seed=rank, dfinal=False)
-    dev = SSDDevice(inp, device=f"cuda:{local}")
+    dev = SSDDevice(inp, device=f"cuda:{local}", extra_flags=step_flags(args))
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev.device)
 
@@ -452,7 +463,8 @@ def run_gpu(args, world, rank, local):
     peaks, src = load_peaks()
     cfg = workload_config(args.workload)
     s_bytes = 2 if inp.dtype == "bf16" else 4
-    model, layer_io = kernel_model(dict(cfg, batch=inp.batch, seqlen=inp.seqlen), s_bytes)
+    model, layer_io = kernel_model(dict(cfg, batch=inp.batch, seqlen=inp.seqlen), s_bytes,
+                                   keep=not args.recompute)
     kernels = {k: {"launches": n, "ms_per_launch": ms / n} for k, (n, ms) in prof.items()
                if not k.startswith("_")}
     launches = sum(v["launches"] for v in kernels.values())
@@ -500,7 +512,9 @@ def run_gpu(args, world, rank, local):
             "dtype": inp.dtype, "data": "synthetic",
             "config": dict(cfg, l2="flushed between steps (256 MB write, outside the events); "
                                    "inputs larger than L2", parallelism="replicas" if world > 1
-                           else "single GPU"),
+                           else "single GPU",
+                           fwd_intermediates="recomputed by the backward" if args.recompute else
+                           "kept by the forward for the backward (SSD_KEEP_FWD_STATES)"),
             "roofline": roof, "layer_roofline": layer, "e2e": e2e,
             "gpu_launches": launches, "kernels": kernels, "clocks": clk,
             "wall_s_timed": t_wall,
@@ -569,7 +583,8 @@ def run_e2e(inp, dev, args, stream):
     import torch
     from mamba_selective_state_gb300.runner import SSDDevice
     nb = E2E_BUFFER_SETS
-    devs = [dev] + [SSDDevice(inp, device=dev.device, dfinal=False) for _ in range(nb - 1)]
+    devs = [dev] + [SSDDevice(inp, device=dev.device, dfinal=False, extra_flags=step_flags(args))
+                    for _ in range(nb - 1)]
     names_in = ["x", "dt", "B", "C", "dy", "dt_bias", "A", "D"]
     if dev.init is not None:
         names_in.append("init")
@@ -883,6 +898,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--recompute", action="store_true",
+                    help="the backward recomputes the forward's intermediates instead of taking "
+                         "the ones the step's forward kept")
     ap.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S,
                     help="least step time in the timed region (0: exactly --steps, for profiling)")
     ap.add_argument("--op", default="ssd", choices=["ssd", "gated_rmsnorm", "context_parallel"])

@@ -73,7 +73,9 @@ typedef enum {
   SSD_ERR_UNSUPPORTED = 2,      /* shape/dtype outside the compiled set, or not an sm_103 device */
   SSD_ERR_WORKSPACE_TOO_SMALL = 3,
   SSD_ERR_CUDA = 4,             /* a CUDA runtime error while enqueuing */
-  SSD_ERR_TIMEOUT = 5           /* a device-side bounded wait expired (read via the status word) */
+  SSD_ERR_TIMEOUT = 5,          /* a device-side bounded wait expired (read via the status word) */
+  SSD_ERR_NO_KEPT_STATES = 6    /* ssd_bwd with SSD_KEEP_FWD_STATES found no forward intermediates of
+                                   this problem in the workspace (read via the status word) */
 } ssd_status;
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
@@ -83,6 +85,22 @@ enum {
   SSD_HAS_SEQ_IDX = 2,   /* seq_idx is given */
   SSD_HAS_DFINAL = 4,    /* ssd_bwd: dfinal_states (upstream gradient of final_states) is given */
   SSD_WANT_DINIT = 8,    /* ssd_bwd: write dinitial_states */
+  /* Keep the forward's intermediates for the backward (the usual training
+   * step: forward, then backward on the same inputs).  ssd_fwd with this
+   * flag leaves in its workspace what the backward would otherwise
+   * recompute -- dt_eff, the chunk-local cumsums of dt_eff * A, the per-chunk
+   * decays and the carry-in state of every chunk (in the problem's dtype) --
+   * and stamps the workspace with the problem's signature; ssd_fwd without it
+   * clears the stamp.  ssd_bwd with this flag, given that same workspace,
+   * takes them from there instead of recomputing them, where it runs its
+   * single-pass state chains (elsewhere it recomputes as usual and ignores
+   * the flag).  The inputs must be the ones that forward saw: the stamp
+   * covers the problem's shape, not its values.  A workspace without the
+   * stamp of this problem makes the backward report SSD_ERR_NO_KEPT_STATES
+   * in the device status word (its results are then garbage).  Forward
+   * results do not depend on the flag; backward results agree with the
+   * recomputing backward to rounding. */
+  SSD_KEEP_FWD_STATES = 16,
   /* Testing only: the first scan tile of the first state chain never
    * publishes its prefix, so the tiles after it exhaust their bounded wait
    * (0.1 s with this flag, 2 s otherwise) and the call ends with
@@ -145,8 +163,9 @@ int ssd_bwd(const ssd_problem* prob, const void* x, const void* dt, const float*
 const char* ssd_status_string(int status);
 
 /* Synchronises `stream`, then reads the device status word of the last call
- * that used `workspace` (SSD_OK or SSD_ERR_TIMEOUT).  Returns SSD_ERR_CUDA if
- * the synchronisation or the copy fails. */
+ * that used `workspace` (SSD_OK, SSD_ERR_TIMEOUT or SSD_ERR_NO_KEPT_STATES;
+ * a timeout is reported first).  Returns SSD_ERR_CUDA if the
+ * synchronisation or the copy fails. */
 int ssd_read_device_status(const void* workspace, ssd_stream_t stream);
 
 /* Allocation-free forward.  The pages have no counterpart: this is a

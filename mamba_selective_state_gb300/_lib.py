@@ -19,12 +19,14 @@ SSD_ERR_UNSUPPORTED = 2
 SSD_ERR_WORKSPACE_TOO_SMALL = 3
 SSD_ERR_CUDA = 4
 SSD_ERR_TIMEOUT = 5
+SSD_ERR_NO_KEPT_STATES = 6
 SSD_F32 = 0
 SSD_BF16 = 1
 SSD_HAS_INIT = 1
 SSD_HAS_SEQ_IDX = 2
 SSD_HAS_DFINAL = 4
 SSD_WANT_DINIT = 8
+SSD_KEEP_FWD_STATES = 16
 SSD_TEST_DROP_SCAN_PUBLISH = 1 << 16
 SSD_PATH_MULTI_KERNEL = 1 << 17
 SSD_PATH_SINGLE_PASS = 1 << 18

@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(256) dt_cumsum_kernel(Plan p, Bufs f) {
       f.hdr->status = 0;
       f.hdr->ticket_fwd = 0;
       f.hdr->ticket_bwd = 0;
+      if (p.kept_mode == 1) f.hdr->kept_sig = p.kept_sig_write;
     }
   }
   const int c = blockIdx.x, bi = blockIdx.y;
@@ -207,14 +208,19 @@ __global__ void __launch_bounds__(256) param_reduce_kernel(Plan p, Bufs f) {
 // Clears the status word of a call whose kernels do not (the single-pass
 // forward).  A kernel on the call's stream rather than a memset: a memset can
 // be served by a copy engine and queue behind the caller's host copies.
-__global__ void status_reset_kernel(WsHeader* hdr) { hdr->status = 0; }
+// It also writes the kept-intermediates stamp (mode 1) or checks it (mode 2).
+__global__ void status_reset_kernel(WsHeader* hdr, int mode, int sig, int sig_write) {
+  int st = 0;
+  if (mode == 1) hdr->kept_sig = sig_write;
+  if (mode == 2 && hdr->kept_sig != sig) st = kDevNoKept;
+  hdr->status = st;
+}
 
 }  // namespace
 
 cudaError_t launch_status_reset(const Plan& p, const Bufs& f, cudaStream_t s) {
-  (void)p;
   set_kernel_name("status_reset");
-  status_reset_kernel<<<1, 1, 0, s>>>(f.hdr);
+  status_reset_kernel<<<1, 1, 0, s>>>(f.hdr, p.kept_mode, p.kept_sig, p.kept_sig_write);
   return cudaGetLastError();
 }
 

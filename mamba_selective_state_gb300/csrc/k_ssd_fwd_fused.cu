@@ -176,7 +176,8 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
                                                                 const __grid_constant__ CUtensorMap tmX,
                                                                 const __grid_constant__ CUtensorMap tmB,
                                                                 const __grid_constant__ CUtensorMap tmC,
-                                                                const __grid_constant__ CUtensorMap tmY) {
+                                                                const __grid_constant__ CUtensorMap tmY,
+                                                                const __grid_constant__ CUtensorMap tmHin) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const FusedGeom G = fused_geom(p.N);
@@ -196,6 +197,9 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
            *b_y = bar + 8, *b_ystg = bar + 9, *b_full = bar + 10, *b_empty = bar + 13;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 16);
   const long long bh = (long long)bi * p.H + h;
+  // keep the intermediates the backward would recompute (dt_eff, chunk
+  // cumsums, per-chunk decays, bf16 carry-in states) in the workspace
+  const bool keep = (p.flags & SSD_KEEP_FWD_STATES) != 0;
 
   if (tid == kCtl) {
     for (int k = 0; k < 3; ++k) mbar_init(&b_x[k], 1);
@@ -253,6 +257,10 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
         wait_or_flag(b_hin, ph, ok);
         wait_or_flag(b_xs, ph, ok);
         tc_fence_after();
+        if (keep) {  // the carry-in state of chunk c, as the products read it
+          tma_store_4d(&tmHin, sH, 0, 0, c, (int)bh);
+          bulk_commit();
+        }
         // group 1: C B^T, S^T = B^T (w . X), Y2 = C H_in^T
         for (int ks = 0; ks < p.N / 16; ++ks) {
           const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
@@ -267,6 +275,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
           const uint64_t dx = smem_desc(smem_u32(sXs) + ks * 2048, 16, 1024, kSwz128);
           mma_bf16(tS, da, dx, idS, ks > 0);
         }
+        if (keep) bulk_wait_read<0>();  // the carry update of chunk c rewrites the tile
         mma_commit(b_m1);
         // y of the previous chunk: store it from its x tile, then refill
         // that tile with the chunk after next
@@ -383,8 +392,17 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
           S.s[rb - 1][j] = (in && j < 32 * rb) ? __expf(lref[rb] - lv[k]) * de[k] : 0.0f;
         S.sd[j] = (in && diag_ok) ? __expf(lref[lane >> 3] - lv[k]) * de[k] : 0.0f;
       }
+      if (keep) {
+        const long long base = bh * p.Lp + t0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          f.dte[base + 4 * lane + k] = de[k];
+          f.lcs[base + 4 * lane + k] = lv[k];
+        }
+      }
       if (lane == 0) {
         S.a_c = (seg_last == seg_in) ? expf(l_last) : 0.0f;
+        if (keep) f.achunk[bh * p.nc + c] = S.a_c;
         S.one_seg = (seg_first == seg_last) ? 1 : 0;
         S.len = len;
         S.fact = (fact_ok && seg_first == seg_last) ? 1 : 0;
@@ -569,7 +587,7 @@ bool ssd_fwd_fused_supported(const Plan& p) {
 cudaError_t launch_ssd_fwd_fused(const Plan& p, const Bufs& f, cudaStream_t s) {
   set_kernel_name("ssd_fwd_fused");
   const FusedGeom G = fused_geom(p.N);
-  CUtensorMap tmX, tmB, tmC, tmY;
+  CUtensorMap tmX, tmB, tmC, tmY, tmHin;
   const uint64_t dxx[4] = {64, (uint64_t)p.H, (uint64_t)p.L, (uint64_t)p.b};
   const uint64_t sxx[3] = {128, (uint64_t)p.H * 128, (uint64_t)p.L * p.H * 128};
   const uint32_t bxx[4] = {64, 1, (uint32_t)kQ, 1};
@@ -581,10 +599,17 @@ cudaError_t launch_ssd_fwd_fused(const Plan& p, const Bufs& f, cudaStream_t s) {
       !encode_tmap_bf16_4d(&tmC, f.C, dbc, sbc, bbc, 128) ||
       !encode_tmap_bf16_4d(&tmY, f.y, dxx, sxx, bxx, 128))
     return cudaErrorInvalidValue;
+  // carry-in states (b, H, nc, N, P) bf16: one (N x 64) tile per chunk
+  const uint64_t dhs[4] = {64, (uint64_t)p.N, (uint64_t)p.nc, (uint64_t)p.b * p.H};
+  const uint64_t shs[3] = {128, (uint64_t)p.N * 128, (uint64_t)p.nc * p.N * 128};
+  const uint32_t bhs[4] = {64, (uint32_t)p.N, 1, 1};
+  if ((p.flags & SSD_KEEP_FWD_STATES) ? !encode_tmap_bf16_4d(&tmHin, f.Hin, dhs, shs, bhs, 128) : false)
+    return cudaErrorInvalidValue;
+  if (!(p.flags & SSD_KEEP_FWD_STATES)) tmHin = tmY;  // unused
   const size_t smem = 1024 + G.bytes;
   cudaError_t e = cudaFuncSetAttribute(ssd_fwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  ssd_fwd_fused_kernel<<<p.b * p.H, kThr, smem, s>>>(p, f, tmX, tmB, tmC, tmY);
+  ssd_fwd_fused_kernel<<<p.b * p.H, kThr, smem, s>>>(p, f, tmX, tmB, tmC, tmY, tmHin);
   return cudaGetLastError();
 }
 

@@ -47,7 +47,7 @@ int make_plan(const ssd_problem* pr, Plan* p) {
     return SSD_ERR_INVALID_ARGUMENT;
   if (pr->nheads % pr->ngroups != 0) return SSD_ERR_INVALID_ARGUMENT;
   if (pr->dtype != SSD_F32 && pr->dtype != SSD_BF16) return SSD_ERR_INVALID_ARGUMENT;
-  if (pr->flags & ~(SSD_HAS_INIT | SSD_HAS_SEQ_IDX | SSD_HAS_DFINAL | SSD_WANT_DINIT |
+  if (pr->flags & ~(SSD_HAS_INIT | SSD_HAS_SEQ_IDX | SSD_HAS_DFINAL | SSD_WANT_DINIT | SSD_KEEP_FWD_STATES |
                     SSD_TEST_DROP_SCAN_PUBLISH | SSD_PATH_MULTI_KERNEL | SSD_PATH_SINGLE_PASS))
     return SSD_ERR_INVALID_ARGUMENT;
   if (pr->chunk_size > 256 || pr->chunk_size % 16 != 0) return SSD_ERR_UNSUPPORTED;
@@ -79,6 +79,18 @@ int make_plan(const ssd_problem* pr, Plan* p) {
   p->hpg = p->H / p->G;
   p->dtype = pr->dtype;
   p->flags = pr->flags;
+  {
+    // FNV-1a over the shape, the evaluation chunk and the inputs' presence
+    uint32_t hsh = 2166136261u;
+    const int64_t keys[] = {pr->batch, pr->seqlen, pr->nheads, pr->headdim, pr->dstate, pr->ngroups,
+                            (int64_t)p->Q, (int64_t)pr->dtype,
+                            (int64_t)(pr->flags & (SSD_HAS_INIT | SSD_HAS_SEQ_IDX))};
+    for (int64_t k : keys)
+      for (int byte = 0; byte < 8; ++byte) hsh = (hsh ^ (uint32_t)((k >> (8 * byte)) & 0xff)) * 16777619u;
+    p->kept_sig = (int)(hsh == 0 ? 1u : hsh);
+    p->kept_mode = 0;
+    p->kept_sig_write = 0;
+  }
   p->Lp = (long long)p->nc * p->Q;
   p->sp_neblk = (p->PN + kSpElems - 1) / kSpElems;
   p->sp_nseg = (p->nc + kSpSegF - 1) / kSpSegF;
@@ -234,6 +246,11 @@ int ssd_fwd(const ssd_problem* prob, const void* x, const void* dt, const float*
   f.init = initial_states; f.seq = seq_idx; f.y = y; f.final_states = final_states;
   bind_workspace(p, workspace, false, &f);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // every forward writes the kept-intermediates stamp: this problem's
+  // signature if it keeps them (both paths leave them in the workspace),
+  // else none
+  p.kept_mode = 1;
+  p.kept_sig_write = (p.flags & SSD_KEEP_FWD_STATES) ? p.kept_sig : 0;
   if (use_fused_fwd(p)) {
     // no scan flags or tickets to reset, only the status word
     SSD_LAUNCH(launch_status_reset(p, f, s));
@@ -280,14 +297,22 @@ int ssd_bwd(const ssd_problem* prob, const void* x, const void* dt, const float*
   f.final_states = nullptr;  // the recomputed forward does not write final_states
   bind_workspace(p, workspace, true, &f);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // recompute the forward intermediates: dt_eff, chunk cumsums, carry-in states
-  SSD_LAUNCH(launch_dt_cumsum(p, f, s));
   if (use_state_chains(p)) {
     // one pass per chain, forward then reverse (16 dL/da_c slots per chunk)
     p.da_nsum = 16;
-    SSD_LAUNCH(launch_state_chain(p, f, false, s));
+    if (p.flags & SSD_KEEP_FWD_STATES) {
+      // dt_eff, the chunk cumsums and decays and the carry-in states are the
+      // forward's: check the stamp (in the status word) instead of recomputing
+      p.kept_mode = 2;
+      SSD_LAUNCH(launch_status_reset(p, f, s));
+    } else {
+      SSD_LAUNCH(launch_dt_cumsum(p, f, s));
+      SSD_LAUNCH(launch_state_chain(p, f, false, s));
+    }
     SSD_LAUNCH(launch_state_chain(p, f, true, s));
   } else {
+    // recompute the forward intermediates: dt_eff, chunk cumsums, carry-in states
+    SSD_LAUNCH(launch_dt_cumsum(p, f, s));
     SSD_LAUNCH(launch_chunk_state(p, f, false, s));
     SSD_LAUNCH(launch_state_passing(p, f, false, true, s));
     // gradient of the carry-in states from y, then the reverse state-passing scan
@@ -308,6 +333,7 @@ const char* ssd_status_string(int status) {
     case SSD_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case SSD_ERR_CUDA: return "CUDA error";
     case SSD_ERR_TIMEOUT: return "device-side wait timed out";
+    case SSD_ERR_NO_KEPT_STATES: return "no kept forward intermediates of this problem in the workspace";
     default: return "unknown status";
   }
 }
@@ -319,7 +345,8 @@ int ssd_read_device_status(const void* workspace, ssd_stream_t stream) {
   if (cudaMemcpyAsync(&st, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return SSD_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return SSD_ERR_CUDA;
-  return (st & kDevTimeout) ? SSD_ERR_TIMEOUT : SSD_OK;
+  if (st & kDevTimeout) return SSD_ERR_TIMEOUT;
+  return (st & kDevNoKept) ? SSD_ERR_NO_KEPT_STATES : SSD_OK;
 }
 
 const char* ssd_version(void) { return "libssd 0.1 sm_103a"; }

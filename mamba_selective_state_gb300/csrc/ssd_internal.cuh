@@ -11,7 +11,7 @@
 namespace ssd {
 
 // Status bits the kernels OR into the device status word.
-enum : int { kDevTimeout = 1 };
+enum : int { kDevTimeout = 1, kDevNoKept = 2 };
 
 // State-passing scan tiling: one CTA scans kSpElems consecutive state elements
 // (kSpThreads threads x 4 floats) over a segment of consecutive chunks:
@@ -28,7 +28,8 @@ struct WsHeader {
   int status;
   int ticket_fwd;
   int ticket_bwd;
-  int pad[61];
+  int kept_sig;  // signature of the problem whose forward intermediates the workspace holds, or 0
+  int pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
@@ -36,6 +37,10 @@ struct Plan {
   // dimensions
   int b, L, H, P, N, G, Q, nc, PN, hpg;  // hpg = heads per group
   int dtype, flags;
+  // nonzero signature of the problem's shape (the kept-intermediates stamp)
+  // and what the launch that resets the status word does with the stamp:
+  // 0 leave it, 1 write kept_sig_write, 2 check it against kept_sig
+  int kept_sig, kept_mode, kept_sig_write;
   long long Lp;                          // nc * Q (padded tokens per row)
   // state-passing scan tiling
   int sp_neblk, sp_nseg, sp_nseg_b, sp_nslot, sp_chains;  // chains = b * H * neblk; nslot = max segments

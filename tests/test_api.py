@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert "sm_103a" in lib.version()
-    for code in range(6):
+    for code in range(7):
         assert lib.status_string(code) and lib.status_string(code) != "unknown status"
     assert lib.status_string(99) == "unknown status"
 
@@ -59,6 +59,10 @@ def test_workspace_sizes(lib):
     nc = 3
     assert fw >= 2 * 2 * 8 * nc * 64 * 128 * 4
     assert lib.ssd_fwd_workspace_bytes(prob(lib, seqlen=385)) > fw   # one more chunk
+    # keeping the forward's intermediates needs no more: they sit where the
+    # backward's recompute puts them
+    keep = prob(lib, flags=lib.SSD_KEEP_FWD_STATES)
+    assert lib.ssd_fwd_workspace_bytes(keep) == fw and lib.ssd_bwd_workspace_bytes(keep) == bw
 
 
 @pytest.mark.parametrize("bad", [

@@ -70,6 +70,12 @@ SMALL = {
                                       dstate=128, ngroups=1, chunk=128, dtype="bf16", init=True,
                                       dfinal=True, seq_lengths=[128, 256, 1, 127, 128, 17]),
     # chunk 32: tensor-core chunk states next to the CUDA-core scan and backward
+    # two chunks, and exactly four (every x tile of the single-pass forward
+    # used once, no refill)
+    "bf16_two_chunks": dict(batch=1, seqlen=200, nheads=2, headdim=64, dstate=128, ngroups=1,
+                            chunk=128, dtype="bf16", init=True),
+    "bf16_four_chunks_exact": dict(batch=2, seqlen=512, nheads=2, headdim=64, dstate=64, ngroups=2,
+                                   chunk=128, dtype="bf16", dfinal=True),
     "bf16_Q32_mixed": dict(batch=1, seqlen=32 * 9 + 11, nheads=4, headdim=64, dstate=64,
                            ngroups=2, chunk=32, dtype="bf16", init=True, dfinal=True,
                            seq_lengths=[100, 199]),
@@ -86,7 +92,8 @@ def test_small_parity(name):
 
 # bf16, headdim 64, d_state 64 or 128: the single-pass forward's shape set
 SINGLE_PASS = ["bf16_N128_G2", "bf16_N64_G4_varlen", "bf16_Q256_init", "bf16_single_token",
-               "bf16_shorter_than_chunk", "bf16_Q32_mixed", "bf16_chunk_aligned_resets"]
+               "bf16_shorter_than_chunk", "bf16_Q32_mixed", "bf16_chunk_aligned_resets", "bf16_two_chunks",
+               "bf16_four_chunks_exact"]
 
 
 @pytest.mark.parametrize("name", SINGLE_PASS)
@@ -126,6 +133,61 @@ def test_single_pass_positive_decay_rate():
     inp.A[1] = 0.01
     _, got = run_device(inp, extra_flags=_lib.SSD_PATH_SINGLE_PASS)
     assert_close(got, oracle_full(inp), inp.dtype)
+
+
+# shapes of the single-pass forward and the state chains, where the backward
+# takes the intermediates the forward kept
+KEPT = ["bf16_N128_G2", "bf16_N64_G4_varlen", "bf16_chunk_aligned_resets", "bf16_four_chunks_exact",
+        "bf16_shorter_than_chunk"]
+
+
+@pytest.mark.parametrize("name", KEPT)
+def test_kept_forward_intermediates(name):
+    """Forward with SSD_KEEP_FWD_STATES, then the backward that takes its
+    dt_eff, chunk cumsums, decays and carry-in states instead of recomputing
+    them: against the oracle, and against the recomputing backward."""
+    from mamba_selective_state_gb300 import _lib
+    inp = make_inputs(seed=12, **SMALL[name])
+    sp = _lib.SSD_PATH_SINGLE_PASS
+    _, kept = run_device(inp, extra_flags=sp | _lib.SSD_KEEP_FWD_STATES)
+    assert_close(kept, oracle_full(inp), inp.dtype)
+    _, rec = run_device(inp, extra_flags=sp)
+    # the forward does not depend on the flag; the gradients agree to rounding
+    assert torch.equal(kept["y"], rec["y"]) and torch.equal(kept["final_states"], rec["final_states"])
+    for k in kept:
+        scale = float(rec[k].abs().max()) or 1.0
+        assert float((kept[k] - rec[k]).abs().max()) <= 1e-2 * scale, k
+
+
+def test_kept_forward_intermediates_on_the_multi_kernel_path():
+    """Where the backward does not run the state chains it recomputes and
+    ignores the flag (its forward still stamps the workspace)."""
+    from mamba_selective_state_gb300 import _lib
+    inp = make_inputs(seed=13, **SMALL["bf16_N128_G2"])
+    _, got = run_device(inp, extra_flags=_lib.SSD_PATH_MULTI_KERNEL | _lib.SSD_KEEP_FWD_STATES)
+    assert_close(got, oracle_full(inp), inp.dtype)
+
+
+def test_missing_kept_intermediates_are_reported():
+    """A backward told to take the forward's intermediates from a workspace
+    whose last forward did not keep them reports SSD_ERR_NO_KEPT_STATES in
+    the status word; the next kept forward and backward are clean again."""
+    from mamba_selective_state_gb300 import _lib
+    from mamba_selective_state_gb300.runner import SSDDevice
+    inp = make_inputs(seed=14, **SMALL["bf16_N64_G4_varlen"])
+    flags = _lib.SSD_PATH_SINGLE_PASS | _lib.SSD_KEEP_FWD_STATES
+    dev = SSDDevice(inp, device="cuda", extra_flags=flags)
+    dev.fwd_prob.flags &= ~_lib.SSD_KEEP_FWD_STATES   # a forward that keeps nothing
+    dev.fwd()
+    dev.fwd_prob.flags |= _lib.SSD_KEEP_FWD_STATES
+    dev.bwd()
+    torch.cuda.synchronize()
+    assert dev.device_status() == _lib.SSD_ERR_NO_KEPT_STATES
+    assert "kept" in _lib.status_string(_lib.SSD_ERR_NO_KEPT_STATES)
+    dev.fwd()
+    dev.bwd()
+    torch.cuda.synchronize()
+    assert dev.device_status() == 0
 
 
 def test_null_init_equals_zero_init():
