@@ -7,16 +7,18 @@
 // owns one chain and, per chunk of kQ = 128 tokens:
 //
 //   dt_eff_j = softplus(dt_j + dt_bias_h),  l_i = sum_{k<=i} dt_eff_k A_h   (chunk-local)
-//   CB       = C B^T                                   (tensor cores, TMEM)
+//   [CB | Y2] = C [B ; H_in]^T                          (tensor cores, TMEM)
 //   A_hat_ij = CB_ij exp(l_i - l_j) dt_eff_j  [j <= i, same sequence]
-//   Y1       = A_hat X,   Y2 = C H_in^T                 (tensor cores)
+//   Y1       = A_hat X                                  (tensor cores)
 //   y_i      = Y1_i + cv_i exp(l_i) Y2_i + D_h x_i
 //   S^T      = B^T (w . X),  w_j = exp(l_last - l_j) dt_eff_j [seg_j = seg_last]
 //   H_in     <- a_c H_in + S   (a_c = exp(l_last), 0 when a sequence starts in the chunk)
 //
 // with the carry H_in held in fp32 registers of the compute warps (one
 // d_state row per TMEM lane, 16 headdim columns per thread) and handed to the
-// tensor core as a bf16 tile in shared memory.  The recurrence is the one of
+// tensor core as bf16 rows stacked under the B tile: C B^T and Y2 = C H_in^T
+// share their A operand, so one N = 192 product forms both (a tcgen05.mma of
+// N <= 128 costs about as much as one of N = 192).  The recurrence is the one of
 // the chunked evaluation (page "llm-mamba-200", sections 1-3); the chunk
 // length is internal to this kernel (the result does not depend on it).
 //
@@ -70,27 +72,28 @@ struct alignas(16) Slot {
   float lref[4];
 };
 
-__host__ __device__ inline uint32_t r1024(uint32_t v) { return (v + 1023u) & ~1023u; }
-
 struct FusedGeom {
   int ncb;          // 64-column blocks of B/C along d_state
-  uint32_t cblk;    // bytes of one B/C column block (kQ rows x 128 B)
-  uint32_t offX, offB, offC, offXs, offA, offH, offSl, offBar, bytes;
+  uint32_t cblk;    // bytes of one C column block (kQ rows x 128 B)
+  uint32_t bhblk;   // bytes of one [B ; H_in] column block (kQ + 64 rows x 128 B)
+  uint32_t offX, offB, offC, offXs, offA, offSl, offBar, bytes;
 };
 
 __host__ __device__ inline FusedGeom fused_geom(int N) {
   FusedGeom g;
   g.ncb = N / 64;
   g.cblk = kQ * 128u;
+  g.bhblk = (kQ + 64) * 128u;
   g.offX = 0;
+  // [B ; H_in] blocks: the chunk's 128 B rows, then the 64 headdim rows of
+  // the carry-in state (K = d_state in both)
   g.offB = g.offX + kXbuf * g.cblk;
   // with d_state 64 the product B^T (w . X) reads a second (unused) 64-row
-  // block of A past the B tile: the C tile
-  g.offC = g.offB + g.ncb * g.cblk;
+  // block of A past the [B ; H_in] block: the C tile
+  g.offC = g.offB + g.ncb * g.bhblk;
   g.offXs = g.offC + g.ncb * g.cblk;
   g.offA = g.offXs + g.cblk;
-  g.offH = g.offA + 2u * g.cblk;
-  g.offSl = g.offH + r1024((uint32_t)N * 128u);
+  g.offSl = g.offA + 2u * g.cblk;
   g.offBar = g.offSl + (uint32_t)(kRing * sizeof(Slot) + 255) / 256u * 256u;
   g.bytes = g.offBar + 256u;
   return g;
@@ -176,8 +179,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
                                                                 const __grid_constant__ CUtensorMap tmX,
                                                                 const __grid_constant__ CUtensorMap tmB,
                                                                 const __grid_constant__ CUtensorMap tmC,
-                                                                const __grid_constant__ CUtensorMap tmY,
-                                                                const __grid_constant__ CUtensorMap tmHin) {
+                                                                const __grid_constant__ CUtensorMap tmY) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const FusedGeom G = fused_geom(p.N);
@@ -186,11 +188,10 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nch = (p.L + kQ - 1) / kQ;
   uint8_t* sX = sm + G.offX;     // [kXbuf] x tiles; y is staged in place
-  uint8_t* sB = sm + G.offB;
+  uint8_t* sB = sm + G.offB;     // [B ; H_in] blocks
   uint8_t* sC = sm + G.offC;
   uint8_t* sXs = sm + G.offXs;   // w . X
   uint8_t* sA = sm + G.offA;     // A_hat, two 64-column blocks
-  uint8_t* sH = sm + G.offH;     // carry-in state, (d_state rows, 64 bf16)
   Slot* ring = reinterpret_cast<Slot*>(sm + G.offSl);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + G.offBar);
   uint64_t *b_x = bar, *b_bc = bar + 3, *b_hin = bar + 4, *b_xs = bar + 5, *b_m1 = bar + 6, *b_ahat = bar + 7,
@@ -225,7 +226,8 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tmem_slot;
-  const uint32_t tCB = tm, tS = tm + 128, tY1 = tm + 192, tY2 = tm + 256;  // tY2: [2] x 64
+  // [CB | Y2] double-buffered (2 x 192 columns) | S^T | Y1
+  const uint32_t tCBY = tm, tS = tm + 384, tY1 = tm + 448;
   bool ok = true;
 
   if (warp == kCtl / 32) {
@@ -240,11 +242,11 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
       auto load_bc = [&](int c) {
         mbar_expect_tx(b_bc, G.ncb * 2u * G.cblk);
         for (int q = 0; q < G.ncb; ++q) {
-          tma_load_4d(sB + q * G.cblk, &tmB, b_bc, q * 64, g, c * kQ, bi);
+          tma_load_4d(sB + q * G.bhblk, &tmB, b_bc, q * 64, g, c * kQ, bi);
           tma_load_4d(sC + q * G.cblk, &tmC, b_bc, q * 64, g, c * kQ, bi);
         }
       };
-      const uint32_t id128 = idesc_bf16(128, 128, 0, 0);  // K-major A and B
+      const uint32_t id192 = idesc_bf16(128, 192, 0, 0);  // K-major A and B
       const uint32_t id64b = idesc_bf16(128, 64, 0, 1);   // K-major A, MN-major B
       const uint32_t idS = idesc_bf16(128, 64, 1, 1);     // MN-major A and B
       load_x(0);
@@ -257,25 +259,18 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
         wait_or_flag(b_hin, ph, ok);
         wait_or_flag(b_xs, ph, ok);
         tc_fence_after();
-        if (keep) {  // the carry-in state of chunk c, as the products read it
-          tma_store_4d(&tmHin, sH, 0, 0, c, (int)bh);
-          bulk_commit();
-        }
-        // group 1: C B^T, S^T = B^T (w . X), Y2 = C H_in^T
+        // group 1: [C B^T | Y2 = C H_in^T], S^T = B^T (w . X)
         for (int ks = 0; ks < p.N / 16; ++ks) {
           const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
           const uint64_t dc = smem_desc(smem_u32(sC) + kb * G.cblk + kin, 16, 1024, kSwz128);
-          const uint64_t db = smem_desc(smem_u32(sB) + kb * G.cblk + kin, 16, 1024, kSwz128);
-          const uint64_t dh = smem_desc(smem_u32(sH) + ks * 2048, 16, 1024, kSwz128);
-          mma_bf16(tCB, dc, db, id128, ks > 0);
-          mma_bf16(tY2 + ph * 64, dc, dh, id64b, ks > 0);
+          const uint64_t dbh = smem_desc(smem_u32(sB) + kb * G.bhblk + kin, 16, 1024, kSwz128);
+          mma_bf16(tCBY + ph * 192, dc, dbh, id192, ks > 0);
         }
         for (int ks = 0; ks < kQ / 16; ++ks) {
-          const uint64_t da = smem_desc(smem_u32(sB) + ks * 2048, G.cblk, 1024, kSwz128);
+          const uint64_t da = smem_desc(smem_u32(sB) + ks * 2048, G.bhblk, 1024, kSwz128);
           const uint64_t dx = smem_desc(smem_u32(sXs) + ks * 2048, 16, 1024, kSwz128);
           mma_bf16(tS, da, dx, idS, ks > 0);
         }
-        if (keep) bulk_wait_read<0>();  // the carry update of chunk c rewrites the tile
         mma_commit(b_m1);
         // y of the previous chunk: store it from its x tile, then refill
         // that tile with the chunk after next
@@ -430,13 +425,24 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
 #pragma unroll
     for (int k = 0; k < 16; ++k)
       hreg[k] = (f.init != nullptr && nvalid) ? f.init[(bh * p.P + p0 + k) * p.N + n] : 0.0f;
-    auto write_h = [&]() {  // bf16 carry tile: row n, columns p0..p0+15
+    // the carry as bf16 rows of the [B ; H_in] blocks: headdim row p, d_state
+    // column n (K-major, like the B rows above it); with the forward's
+    // intermediates kept, also H_in[c] of the chunk to the workspace
+    auto write_h = [&](int c) {
       if (nvalid) {
-        uint32_t w8[8];
+        uint8_t* hb = sB + (n >> 6) * G.bhblk + kQ * 128u;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) w8[e] = pack_bf16x2(hreg[2 * e], hreg[2 * e + 1]);
-        *reinterpret_cast<uint4*>(sH + swz128_off(n, p0)) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
-        *reinterpret_cast<uint4*>(sH + swz128_off(n, p0 + 8)) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+        for (int k = 0; k < 16; ++k)
+          *reinterpret_cast<__nv_bfloat16*>(hb + swz128_off(p0 + k, n & 63)) = __float2bfloat16_rn(hreg[k]);
+        if (keep) {
+          uint32_t w8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w8[e] = pack_bf16x2(hreg[2 * e], hreg[2 * e + 1]);
+          uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(f.Hin) +
+                                                ((bh * p.nc + c) * p.N + n) * 64 + p0);
+          out[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+          out[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+        }
       }
     };
     auto arrive = [&](uint64_t* b) {
@@ -468,7 +474,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
     };
     // prologue: initial carry, the A_hat zeros above the diagonal blocks,
     // w . X of chunk 0
-    write_h();
+    write_h(0);
     fence_async_smem();
     arrive(b_hin);
     for (int q = 2 * sq4 + 2 + wg; q < 8; q += 4) {
@@ -491,7 +497,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
 #pragma unroll
         for (int k = 0; k < 16; ++k) hreg[k] = fmaf(a, hreg[k], sv[k]);
         if (c + 1 < nch) {
-          write_h();
+          write_h(c + 1);
         } else if (f.final_states != nullptr && nvalid) {
 #pragma unroll
           for (int k = 0; k < 16; ++k) f.final_states[(bh * p.P + p0 + k) * p.N + n] = hreg[k];
@@ -510,7 +516,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
           uint32_t pk[8] = {0, 0, 0, 0, 0, 0, 0, 0};
           if (q * 16 < len) {  // warp-uniform
             float v[16];
-            tmem_ld16(tmem_addr(tCB, 32 * sq4, q * 16), v);
+            tmem_ld16(tmem_addr(tCBY + (c & 1) * 192, 32 * sq4, q * 16), v);
             if (S.fact && q < 2 * sq4) {
               unit_fact(v, S.s[sq4 - 1], q * 16, r_row, pk);
             } else if (S.fact_diag) {  // diagonal block, factored within it
@@ -539,7 +545,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
         // shared memory
         uint32_t ar[16], br[16];
         tmem_ld16_issue(tmem_addr(tY1, 32 * sq4, p0), ar);
-        tmem_ld16_issue(tmem_addr(tY2 + (c & 1) * 64, 32 * sq4, p0), br);
+        tmem_ld16_issue(tmem_addr(tCBY + (c & 1) * 192 + 128, 32 * sq4, p0), br);
         const float cv = S.cve[n];
         uint8_t* xt = sX + (c % kXbuf) * G.cblk;
         uint4* x0p = reinterpret_cast<uint4*>(xt + swz128_off(n, p0));
@@ -587,7 +593,7 @@ bool ssd_fwd_fused_supported(const Plan& p) {
 cudaError_t launch_ssd_fwd_fused(const Plan& p, const Bufs& f, cudaStream_t s) {
   set_kernel_name("ssd_fwd_fused");
   const FusedGeom G = fused_geom(p.N);
-  CUtensorMap tmX, tmB, tmC, tmY, tmHin;
+  CUtensorMap tmX, tmB, tmC, tmY;
   const uint64_t dxx[4] = {64, (uint64_t)p.H, (uint64_t)p.L, (uint64_t)p.b};
   const uint64_t sxx[3] = {128, (uint64_t)p.H * 128, (uint64_t)p.L * p.H * 128};
   const uint32_t bxx[4] = {64, 1, (uint32_t)kQ, 1};
@@ -599,17 +605,10 @@ cudaError_t launch_ssd_fwd_fused(const Plan& p, const Bufs& f, cudaStream_t s) {
       !encode_tmap_bf16_4d(&tmC, f.C, dbc, sbc, bbc, 128) ||
       !encode_tmap_bf16_4d(&tmY, f.y, dxx, sxx, bxx, 128))
     return cudaErrorInvalidValue;
-  // carry-in states (b, H, nc, N, P) bf16: one (N x 64) tile per chunk
-  const uint64_t dhs[4] = {64, (uint64_t)p.N, (uint64_t)p.nc, (uint64_t)p.b * p.H};
-  const uint64_t shs[3] = {128, (uint64_t)p.N * 128, (uint64_t)p.nc * p.N * 128};
-  const uint32_t bhs[4] = {64, (uint32_t)p.N, 1, 1};
-  if ((p.flags & SSD_KEEP_FWD_STATES) ? !encode_tmap_bf16_4d(&tmHin, f.Hin, dhs, shs, bhs, 128) : false)
-    return cudaErrorInvalidValue;
-  if (!(p.flags & SSD_KEEP_FWD_STATES)) tmHin = tmY;  // unused
   const size_t smem = 1024 + G.bytes;
   cudaError_t e = cudaFuncSetAttribute(ssd_fwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  ssd_fwd_fused_kernel<<<p.b * p.H, kThr, smem, s>>>(p, f, tmX, tmB, tmC, tmY, tmHin);
+  ssd_fwd_fused_kernel<<<p.b * p.H, kThr, smem, s>>>(p, f, tmX, tmB, tmC, tmY);
   return cudaGetLastError();
 }
 

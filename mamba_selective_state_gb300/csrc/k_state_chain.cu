@@ -175,19 +175,19 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
       int s, sref;
       bool in;
     };
+    // (the loads are unconditional, from clamped addresses, so that they can
+    // land in the registers that use them; the conditions apply at the use)
     auto ld_raw = [&](int k) {
-      Raw r{0.0f, 0.0f, 0.0f, 0, 0, false};
-      if (k < nc) {
-        const int c = chunk_of(k), t0 = c * kQ, len = min(kQ, p.L - t0), row = tid >> 2;
-        r.in = row < len;
-        if (r.in) {
-          r.l = __ldg(lrow + t0 + row);
-          r.d = __ldg(drow + t0 + row);
-          r.lref = kRev ? 0.0f : __ldg(lrow + t0 + len - 1);
-          r.s = seqr ? __ldg(seqr + t0 + row) : 0;
-          r.sref = seqr ? __ldg(seqr + (kRev ? (t0 > 0 ? t0 - 1 : 0) : t0 + len - 1)) : 0;
-        }
-      }
+      Raw r;
+      const int kk = k < nc ? k : nc - 1;
+      const int c = chunk_of(kk), t0 = c * kQ, len = min(kQ, p.L - t0), row = tid >> 2;
+      const int rr = row < len ? row : len - 1;
+      r.in = k < nc && row < len;
+      r.l = __ldg(lrow + t0 + rr);
+      r.d = __ldg(drow + t0 + rr);
+      r.lref = kRev ? 0.0f : __ldg(lrow + t0 + len - 1);
+      r.s = seqr ? __ldg(seqr + t0 + rr) : 0;
+      r.sref = seqr ? __ldg(seqr + (kRev ? (t0 > 0 ? t0 - 1 : 0) : t0 + len - 1)) : 0;
       return r;
     };
     auto make_w = [&](const Raw& r) {
@@ -218,24 +218,23 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
     // reverse: this thread's 16 carry-in values of the next chunk, loaded one
     // chunk ahead (they only enter dL/da_c)
     auto load_h = [&](int k, uint4 (&hv)[2]) {
-      hv[0] = hv[1] = make_uint4(0, 0, 0, 0);
-      if (kRev && hwarp && nvalid && k < nc) {
+      if (kRev && hwarp) {
+        const int kk = k < nc ? k : nc - 1, nn = nvalid ? n : 0;
         const uint4* hp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(f.Hin) +
-                                                         ((bh * nc + chunk_of(k)) * p.N + n) * 64 + p0);
+                                                         ((bh * nc + chunk_of(kk)) * p.N + nn) * 64 + p0);
         hv[0] = hp[0];
         hv[1] = hp[1];
       }
     };
-    uint4 hcur[2];
-    load_h(0, hcur);
-    Raw rnext = ld_raw(1);
-    scale(0, make_w(ld_raw(0)));
-    for (int k = 0; k < nc; ++k) {
-      uint4 hnext[2];
-      load_h(k + 1, hnext);
-      const Raw r2 = ld_raw(k + 2);
-      if (k + 1 < nc) scale(k + 1, make_w(rnext));
-      rnext = r2;
+    // One step: chunk k's value is written out and the product of chunk k
+    // folded in, while w . T1 of chunk k+1 is formed and the operands of the
+    // steps ahead are in flight.  The prefetched registers ping-pong between
+    // two sets (r_use/h_use read here, r_fill/h_fill loaded here and read a
+    // step later), so no copy waits on a load still in flight.
+    auto step = [&](int k, Raw& r_fill, const Raw& r_use, uint4 (&h_fill)[2], const uint4 (&h_use)[2]) {
+      load_h(k + 1, h_fill);
+      r_fill = ld_raw(k + 2);
+      if (k + 1 < nc) scale(k + 1, make_w(r_use));
       const int c = chunk_of(k), b = k & 1;
       const float a = f.achunk[bh * nc + c];
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(kRev ? f.dS : f.Hin) + ((bh * nc + c) * p.N + n) * 64 + p0;
@@ -247,8 +246,8 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
         reinterpret_cast<uint4*>(out)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
         reinterpret_cast<uint4*>(out)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
         if (kRev) {  // dL/da_c partial: <G, H_in[c]> over this thread's 16 entries
-          const uint32_t hw[8] = {hcur[0].x, hcur[0].y, hcur[0].z, hcur[0].w,
-                                  hcur[1].x, hcur[1].y, hcur[1].z, hcur[1].w};
+          const uint32_t hw[8] = {h_use[0].x, h_use[0].y, h_use[0].z, h_use[0].w,
+                                  h_use[1].x, h_use[1].y, h_use[1].z, h_use[1].w};
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[e]));
@@ -272,8 +271,15 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&b_free[b]);
-      hcur[0] = hnext[0];
-      hcur[1] = hnext[1];
+    };
+    // set j & 1 holds the operands of chunk j
+    Raw r0 = ld_raw(0), r1 = ld_raw(1);
+    uint4 h0[2] = {}, h1[2] = {};
+    load_h(0, h0);
+    scale(0, make_w(r0));
+    for (int k = 0; k < nc; k += 2) {
+      step(k, r0, r1, h1, h0);
+      if (k + 1 < nc) step(k + 1, r1, r0, h0, h1);
     }
     if (kRev && f.dinit != nullptr && nvalid) {
 #pragma unroll
