@@ -409,6 +409,14 @@ def run_gpu(args, world, rank, local):
             mid.record(stream)
         dev.bwd(stream=stream)
 
+    # one checked step first: the backward's first kernel resets the status
+    # word, so the forward's own status is read before it runs
+    dev.fwd(stream=stream)
+    if dev.device_status(stream) != 0:
+        raise RuntimeError("device status word reports an error after the forward")
+    dev.bwd(stream=stream)
+    if dev.device_status(stream) != 0:
+        raise RuntimeError("device status word reports an error after the backward")
     w0 = torch.cuda.Event(enable_timing=True)
     w1 = torch.cuda.Event(enable_timing=True)
     for k in range(args.warmup):

@@ -26,6 +26,8 @@ def run_device(inp, **kw):
     from mamba_selective_state_gb300.runner import SSDDevice
     dev = SSDDevice(inp, device="cuda", **kw)
     dev.fwd()
+    # the backward's first kernel resets the status word: read the forward's first
+    assert dev.device_status() == 0
     dev.bwd()
     torch.cuda.synchronize()
     assert dev.device_status() == 0
