@@ -76,7 +76,7 @@ struct FusedGeom {
   int ncb;          // 64-column blocks of B/C along d_state
   uint32_t cblk;    // bytes of one C column block (kQ rows x 128 B)
   uint32_t bhblk;   // bytes of one [B ; H_in] column block (kQ + 64 rows x 128 B)
-  uint32_t offX, offB, offC, offXs, offA, offSl, offBar, bytes;
+  uint32_t offX, offB, offC, offXs, offA, offH, offSl, offBar, bytes;
 };
 
 __host__ __device__ inline FusedGeom fused_geom(int N) {
@@ -93,7 +93,10 @@ __host__ __device__ inline FusedGeom fused_geom(int N) {
   g.offC = g.offB + g.ncb * g.bhblk;
   g.offXs = g.offC + g.ncb * g.cblk;
   g.offA = g.offXs + g.cblk;
-  g.offSl = g.offA + 2u * g.cblk;
+  // the carry-in state as a (d_state rows, 64 bf16) tile for the tensor
+  // store of the kept intermediates
+  g.offH = g.offA + 2u * g.cblk;
+  g.offSl = g.offH + ((uint32_t)N * 128u + 1023u) / 1024u * 1024u;
   g.offBar = g.offSl + (uint32_t)(kRing * sizeof(Slot) + 255) / 256u * 256u;
   g.bytes = g.offBar + 256u;
   return g;
@@ -179,7 +182,8 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
                                                                 const __grid_constant__ CUtensorMap tmX,
                                                                 const __grid_constant__ CUtensorMap tmB,
                                                                 const __grid_constant__ CUtensorMap tmC,
-                                                                const __grid_constant__ CUtensorMap tmY) {
+                                                                const __grid_constant__ CUtensorMap tmY,
+                                                                const __grid_constant__ CUtensorMap tmHin) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const FusedGeom G = fused_geom(p.N);
@@ -192,6 +196,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
   uint8_t* sC = sm + G.offC;
   uint8_t* sXs = sm + G.offXs;   // w . X
   uint8_t* sA = sm + G.offA;     // A_hat, two 64-column blocks
+  uint8_t* sH = sm + G.offH;     // kept carry-in state (d_state rows, 64 bf16)
   Slot* ring = reinterpret_cast<Slot*>(sm + G.offSl);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + G.offBar);
   uint64_t *b_x = bar, *b_bc = bar + 3, *b_hin = bar + 4, *b_xs = bar + 5, *b_m1 = bar + 6, *b_ahat = bar + 7,
@@ -259,6 +264,10 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
         wait_or_flag(b_hin, ph, ok);
         wait_or_flag(b_xs, ph, ok);
         tc_fence_after();
+        if (keep) {  // the carry-in state of chunk c, as the products read it
+          tma_store_4d(&tmHin, sH, 0, 0, c, (int)bh);
+          bulk_commit();
+        }
         // group 1: [C B^T | Y2 = C H_in^T], S^T = B^T (w . X)
         for (int ks = 0; ks < p.N / 16; ++ks) {
           const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
@@ -271,6 +280,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
           const uint64_t dx = smem_desc(smem_u32(sXs) + ks * 2048, 16, 1024, kSwz128);
           mma_bf16(tS, da, dx, idS, ks > 0);
         }
+        if (keep) bulk_wait_read<0>();  // the carry update of chunk c rewrites the tile
         mma_commit(b_m1);
         // y of the previous chunk: store it from its x tile, then refill
         // that tile with the chunk after next
@@ -427,8 +437,9 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
       hreg[k] = (f.init != nullptr && nvalid) ? f.init[(bh * p.P + p0 + k) * p.N + n] : 0.0f;
     // the carry as bf16 rows of the [B ; H_in] blocks: headdim row p, d_state
     // column n (K-major, like the B rows above it); with the forward's
-    // intermediates kept, also H_in[c] of the chunk to the workspace
-    auto write_h = [&](int c) {
+    // intermediates kept, also as row n of the (d_state, headdim) tile that
+    // the control lane stores
+    auto write_h = [&]() {
       if (nvalid) {
         uint8_t* hb = sB + (n >> 6) * G.bhblk + kQ * 128u;
 #pragma unroll
@@ -438,10 +449,8 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
           uint32_t w8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) w8[e] = pack_bf16x2(hreg[2 * e], hreg[2 * e + 1]);
-          uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(f.Hin) +
-                                                ((bh * p.nc + c) * p.N + n) * 64 + p0);
-          out[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
-          out[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+          *reinterpret_cast<uint4*>(sH + swz128_off(n, p0)) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+          *reinterpret_cast<uint4*>(sH + swz128_off(n, p0 + 8)) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
         }
       }
     };
@@ -474,7 +483,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
     };
     // prologue: initial carry, the A_hat zeros above the diagonal blocks,
     // w . X of chunk 0
-    write_h(0);
+    write_h();
     fence_async_smem();
     arrive(b_hin);
     for (int q = 2 * sq4 + 2 + wg; q < 8; q += 4) {
@@ -497,7 +506,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
 #pragma unroll
         for (int k = 0; k < 16; ++k) hreg[k] = fmaf(a, hreg[k], sv[k]);
         if (c + 1 < nch) {
-          write_h(c + 1);
+          write_h();
         } else if (f.final_states != nullptr && nvalid) {
 #pragma unroll
           for (int k = 0; k < 16; ++k) f.final_states[(bh * p.P + p0 + k) * p.N + n] = hreg[k];
@@ -593,7 +602,7 @@ bool ssd_fwd_fused_supported(const Plan& p) {
 cudaError_t launch_ssd_fwd_fused(const Plan& p, const Bufs& f, cudaStream_t s) {
   set_kernel_name("ssd_fwd_fused");
   const FusedGeom G = fused_geom(p.N);
-  CUtensorMap tmX, tmB, tmC, tmY;
+  CUtensorMap tmX, tmB, tmC, tmY, tmHin;
   const uint64_t dxx[4] = {64, (uint64_t)p.H, (uint64_t)p.L, (uint64_t)p.b};
   const uint64_t sxx[3] = {128, (uint64_t)p.H * 128, (uint64_t)p.L * p.H * 128};
   const uint32_t bxx[4] = {64, 1, (uint32_t)kQ, 1};
@@ -605,10 +614,19 @@ cudaError_t launch_ssd_fwd_fused(const Plan& p, const Bufs& f, cudaStream_t s) {
       !encode_tmap_bf16_4d(&tmC, f.C, dbc, sbc, bbc, 128) ||
       !encode_tmap_bf16_4d(&tmY, f.y, dxx, sxx, bxx, 128))
     return cudaErrorInvalidValue;
+  // kept carry-in states (b, H, nc, N, P) bf16: one (N x 64) tile per chunk
+  if (p.flags & SSD_KEEP_FWD_STATES) {
+    const uint64_t dhs[4] = {64, (uint64_t)p.N, (uint64_t)p.nc, (uint64_t)p.b * p.H};
+    const uint64_t shs[3] = {128, (uint64_t)p.N * 128, (uint64_t)p.nc * p.N * 128};
+    const uint32_t bhs[4] = {64, (uint32_t)p.N, 1, 1};
+    if (!encode_tmap_bf16_4d(&tmHin, f.Hin, dhs, shs, bhs, 128)) return cudaErrorInvalidValue;
+  } else {
+    tmHin = tmY;  // unused
+  }
   const size_t smem = 1024 + G.bytes;
   cudaError_t e = cudaFuncSetAttribute(ssd_fwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  ssd_fwd_fused_kernel<<<p.b * p.H, kThr, smem, s>>>(p, f, tmX, tmB, tmC, tmY);
+  ssd_fwd_fused_kernel<<<p.b * p.H, kThr, smem, s>>>(p, f, tmX, tmB, tmC, tmY, tmHin);
   return cudaGetLastError();
 }
 
