@@ -91,7 +91,7 @@ def kernel_model(cfg, dtype_bytes, keep=False):
     # Y_c = C H_in^T and dX = M^T dY; the dB/dC kernel, per head, dM again,
     # dC += dy H, dB += x dS, dC += dCB B and dB += dCB^T C.
     bwd_tok_flops = gunits * 2 * Q * Q * N + units * (4 * Q * Q * P + 4 * Q * P * N)
-    bwd_dbc_flops = units * (2 * Q * Q * P + 4 * Q * N * P + 4 * Q * Q * N)
+    bwd_dbc_flops = units * (2 * Q * Q * P + 4 * Q * N * P) + gunits * 4 * Q * Q * N
     # per-head token gradients (dx, ddt_eff, dl): x, dy, B, C, dS, H_in in; dx out
     m["chunk_bwd"] = dict(bytes=3 * tokx + 2 * tokbc + 2 * stS + 4 * per_tok, flops=bwd_tok_flops)
     # group gradients dB, dC: x, dy, B, C, dS, H_in in; dB, dC out

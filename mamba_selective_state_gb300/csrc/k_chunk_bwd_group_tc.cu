@@ -1,35 +1,32 @@
-// k_chunk_bwd_group_tc.cu -- per-head token gradients of one chunk for all
-// heads of one group, on the 5th-generation tensor cores (chunk <= 128).
+// k_chunk_bwd_group_tc.cu -- dB and dC of one chunk for one group of heads,
+// on the 5th-generation tensor cores (bf16, headdim 64, chunk <= 128).
 //
 // Notation (chunk c, head h, chunk-local tokens i, j):
-//   E_ij = exp(l_i - l_j) [j <= i, seg_i = seg_j],  M_ij = (C_i.B_j) E_ij dt_j,
-//   dM_ij = dy_i . x_j,  R_ij = dM_ij M_ij,  u_j = sv_j exp(l_last - l_j) dt_j.
-// Writes, per head:
-//   dx_j      = sum_i M_ij dy_i + u_j dS B_j + D_h dy_j
-//   ddt_eff_j = sum_i dM_ij (C_i.B_j) E_ij + sv_j exp(l_last - l_j) (x_j . dS B_j)
-//   dl_t      = sum_j R_tj - sum_i R_it + [cv_t] e^{l_t} dy_t . (H C_t) - u_t (x_t . dS B_t)
-// and the per-chunk partials sum_j u_j (x_j . dS B_j) and sum dy . x.
+//   E^h_ij = exp(l^h_i - l^h_j) [j <= i, seg_i = seg_j],   dM^h_ij = dy^h_i . x^h_j,
+//   dCB^h_ij = dM^h_ij E^h_ij dt^h_j,   cv_i = [seg_i = segment live at the carry-in],
+//   u^h_j = [seg_j = seg_last] exp(l^h_last - l^h_j) dt^h_j.
+// The intra-chunk term is linear in dCB and B, C do not depend on the head,
+// so the group's heads are summed before the product:
+//   dC = S B + sum_h diag(cv e^{l^h}) dy^h H^h,
+//   dB = S^T C + sum_h diag(u^h) x^h dS^h,        S = sum_h dCB^h.
+// (page "llm-mamba-200", section on the chunked (SSD) evaluation: the
+// intra-chunk C B^T term and the inter-chunk state terms.)
 //
-// One CTA (512 threads: 16 warps, four per quarter of the tensor-memory
-// lanes) per (chunk, group, batch row).  C B^T does not depend on the head: it
-// is formed once and stays in tensor memory.  For each head of the group
-// (x, dy double-buffered by TMA; dS, H single-buffered):
-//   1. tensor cores: dM = dy x^T (M = i), dXs = B dS^T, Yc = C H^T -- issued
-//      while the previous head's epilogue runs (dXs is double-buffered);
-//   2. the warps read C B^T and dM back (thread = row i; the four warpgroups
-//      split the columns), form E, M, R and dM (C.B) E; row sums stay in the
-//      thread; column sums are taken by a fixed warp-shuffle transpose-reduce
-//      and a fixed-order fold over the lane quarters (bitwise reproducible);
-//      M is written row by row as a bf16 tile that the tensor core reads as
-//      the MN-major A operand of M^T; 16-column blocks that lie wholly above
-//      the diagonal for a warp's 32 rows are skipped;
-//   3. tensor cores: dX = M^T dy (M = j);
-//   4. epilogue (thread = token j): dx, ddt_eff, dl to global memory; the
-//      per-chunk sums are warp butterflies folded in a fixed order.
+// One CTA (16 compute warps + one control warp) per (chunk, group, batch
+// row).  Per head, x/dy and dS/H arrive by tensor copies into double
+// buffers; the tensor core forms dM = dy x^T into one of two tensor-memory
+// buffers; the compute warps scale the x and dy rows in place (u, cv e^l)
+// and the tensor core adds the carry and state terms to the dC, dB
+// accumulators (K = headdim) while the compute warps read dM back (thread =
+// row i, a warpgroup per 32 columns) and add dM o E o dt into S, held in
+// registers across the heads (fp32).  After the last head S is written once
+// as a bf16 tile and two products (K = 128 tokens) finish dC and dB.  Blocks
+// of S strictly below a warp's diagonal block use the factored decay
+// exp(l_i - l_r) exp(l_r - l_j) (both <= 1 when A_h <= 0 and the chunk holds
+// one sequence); blocks wholly above the diagonal are skipped.
 // (page "B200 Helion Mamba-2" (aitrends.kr/articles/109906), section "Helion
 // based B200 kernel redesign": TMA, TMEM and warp specialisation on
-// Blackwell; page "flashinfer PR 6997 Cake RMSNorm" (blog.secrett2633.cloud),
-// section "Fixed-order Tree Fold Reduction": deterministic reductions.)
+// Blackwell.)
 #include "ssd_internal.cuh"
 #include "tc_common.cuh"
 #include "tma_host.h"
@@ -42,7 +39,7 @@ using namespace tc;
 
 constexpr int kRows = 128;
 constexpr int kCompute = 512;        // 16 compute warps: four read each quarter of the TMEM lanes
-constexpr int kThr = kCompute + 32;   // dB/dC kernel: and one control warp for the copies and MMAs
+constexpr int kThr = kCompute + 32;  // and one control warp for the copies and MMAs
 constexpr uint32_t kTok = kRows * 128u;  // one (128 tokens x 64) bf16 tile
 
 __host__ __device__ inline uint32_t r1024(uint32_t v) { return (v + 1023u) & ~1023u; }
@@ -50,9 +47,12 @@ __host__ __device__ inline uint32_t r1024(uint32_t v) { return (v + 1023u) & ~10
 struct GTiles {
   int rows, cw, ncb;
   uint32_t cblk, cswz, cbytes, sbytes;
-  uint32_t offB, offC, offA, offX, offY, offS, offH, offF;
+  uint32_t offB, offC, offX, offY, offS, offH, offF;
 };
 
+// Shared memory: B, C (the final products), x[2], dy[2] (contiguous: the
+// S tile and the dB/dC staging reuse them once every head is done), dS[2],
+// H[2], then the scalars.
 __host__ __device__ inline GTiles gtiles(int N, int Q) {
   GTiles t;
   t.rows = Q < kRows ? Q : kRows;
@@ -64,13 +64,20 @@ __host__ __device__ inline GTiles gtiles(int N, int Q) {
   t.sbytes = r1024((uint32_t)N * 128u);
   t.offB = 0;
   t.offC = t.cbytes;
-  t.offA = 2 * t.cbytes;              // M tile, 128 x 128 bf16 (two 64-column blocks)
-  t.offX = t.offA + 2 * kTok;         // [2] x tiles
-  t.offY = t.offX + 2 * kTok;         // [2] dy tiles
-  t.offS = t.offY + 2 * kTok;         // dS tile
-  t.offH = t.offS + t.sbytes;         // H tile
-  t.offF = t.offH + t.sbytes;
+  t.offX = 2 * t.cbytes;
+  t.offY = t.offX + 2 * kTok;
+  t.offS = t.offY + 2 * kTok;
+  t.offH = t.offS + 2 * t.sbytes;
+  t.offF = t.offH + 2 * t.sbytes;
   return t;
+}
+
+constexpr int kBars = 15;
+
+// Scalars after the tiles: l and dt of two heads, the segment ids, the
+// factor table; then the barriers and the tensor-memory address.
+__host__ __device__ inline size_t group_smem_bytes(const GTiles& T, int Q) {
+  return 1024 + T.offF + (size_t)9 * Q * 4 + kBars * 8 + 16;
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -100,26 +107,10 @@ __device__ __forceinline__ void zero_padding(const GTiles& T, uint8_t* sXb, uint
   }
 }
 
-// Shared-memory bytes: the tiles, then l and dt of two heads, the segment
-// ids, the partial-sum arrays of the token kernel, the barriers and the D of
-// the group's heads.
-__host__ __device__ inline size_t group_smem_bytes(const GTiles& T, int Q, int hpg) {
-  return 1024 + T.offF + (size_t)(5 * Q + 24 * kRows + 8) * 4 + 10 * 8 + 16 + (size_t)hpg * 4 + 16;
-}
-
 __device__ __forceinline__ void named_sync_compute() {  // the 16 compute warps only
   asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
 }
 
-// dB, dC of one chunk for one group (chunk <= 128): one CTA per (chunk,
-// group, batch row) accumulates, in tensor memory and in fixed head order,
-//   dC = sum_h [ dCB_h B + diag(cv e^{l_h}) dy_h H_h ],
-//   dB = sum_h [ dCB_h^T C + diag(u_h) x_h dS_h ],   dCB_h = dM_h o E_h o dt_h.
-// Warp-specialised like the token kernel: the control warp issues dM = dy x^T
-// one head ahead; once it has run, the 16 compute warps scale the x and dy
-// tiles by their row factors in place and the control warp issues the carry
-// and state MMAs, while the compute warps form dCB (thread = row i) as a bf16
-// tile that is the K-major A of dCB B and the MN-major A of dCB^T C.
 __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p, Bufs f,
                                                                         const __grid_constant__ CUtensorMap tmX,
                                                                         const __grid_constant__ CUtensorMap tmY,
@@ -134,21 +125,23 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
   const GTiles T = gtiles(p.N, p.Q);
   uint8_t* sB = sm + T.offB;
   uint8_t* sC = sm + T.offC;
-  uint8_t* sA = sm + T.offA;  // the dCB tile
   uint8_t* sXb = sm + T.offX;
   uint8_t* sYb = sm + T.offY;
-  uint8_t* sS = sm + T.offS;
-  uint8_t* sH = sm + T.offH;
+  uint8_t* sSb = sm + T.offS;
+  uint8_t* sHb = sm + T.offH;
+  uint8_t* sA = sXb;  // the S tile, once the heads are done (two 64-column blocks)
   float* lq = reinterpret_cast<float*>(sm + T.offF);  // [2 slots][Q]
   float* dtq = lq + 2 * p.Q;                          // [2 slots][Q]
   int* sq = reinterpret_cast<int*>(dtq + 2 * p.Q);    // [Q]
-  // ld_bc, xy[2], sh, dm (dM done), cs (carry/state MMAs done), dbc (dB/dC MMAs done),
-  // scaled (x, dy scaled in place), dcb (dCB tile written; dM read back)
-  float* sfac = reinterpret_cast<float*>(sq + p.Q);   // [3][Q] exp(l_{32 rb} - l_j) dt_j, rb = 1..3
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sq + p.Q + 24 * kRows + 8);
-  uint64_t *b_bc = bar, *b_xy = bar + 1, *b_sh = bar + 3, *b_dm = bar + 4, *b_cs = bar + 5, *b_dbc = bar + 6,
-           *b_sc = bar + 7, *b_dcb = bar + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
+  float* sfac = reinterpret_cast<float*>(sq + p.Q);   // [4][Q] exp(l_{32 rb} - l_j) dt_j, j < 32 rb + 32
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sfac + 4 * p.Q);
+  // bc: B, C loaded; xy[2], sh[2]: x/dy and dS/H buffers loaded; dm[2]: dM
+  // in tensor-memory buffer k done; sc[2]: x, dy in buffer k scaled in
+  // place; cs: carry/state MMAs done; dcb[2]: dM buffer k read back; fre:
+  // every head's copies consumed; afin: S tile written; fin: final MMAs done
+  uint64_t *b_bc = bar, *b_xy = bar + 1, *b_sh = bar + 3, *b_dm = bar + 5, *b_sc = bar + 7, *b_cs = bar + 9,
+           *b_dcb = bar + 10, *b_fre = bar + 12, *b_afin = bar + 13, *b_fin = bar + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kBars);
 
   const int c = blockIdx.x, g = blockIdx.y, bi = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -168,22 +161,25 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
     tma_load_4d(sYb + buf * kTok, &tmY, &b_xy[buf], 0, h, t0, bi);
   };
   auto issue_sh = [&](int hh) {
-    const int h = h_first + hh;
-    mbar_expect_tx(b_sh, 2 * s_bytes);
-    tma_load_4d(sS, &tmS, b_sh, 0, 0, c, bi * p.H + h);
-    tma_load_4d(sH, &tmH, b_sh, 0, 0, c, bi * p.H + h);
+    const int buf = hh & 1, h = h_first + hh;
+    mbar_expect_tx(&b_sh[buf], 2 * s_bytes);
+    tma_load_4d(sSb + buf * T.sbytes, &tmS, &b_sh[buf], 0, 0, c, bi * p.H + h);
+    tma_load_4d(sHb + buf * T.sbytes, &tmH, &b_sh[buf], 0, 0, c, bi * p.H + h);
   };
   if (tid == kCompute) {  // the control lane starts the tile copies first
-    for (int k = 0; k < 4; ++k) mbar_init(&bar[k], 1);
+    for (int k = 0; k < kBars; ++k) mbar_init(&bar[k], 1);
     mbar_fence_init();
+    issue_xy(0);
+    issue_sh(0);
+    if (hpg > 1) {
+      issue_xy(1);
+      issue_sh(1);
+    }
     mbar_expect_tx(b_bc, 2 * c_bytes);
     for (int q = 0; q < T.ncb; ++q) {
       tma_load_4d(sB + q * T.cblk, &tmB, b_bc, q * 64, g, t0, bi);
       tma_load_4d(sC + q * T.cblk, &tmC, b_bc, q * 64, g, t0, bi);
     }
-    issue_xy(0);
-    if (hpg > 1) issue_xy(1);
-    issue_sh(0);
   }
   for (int t = tid; t < p.Q; t += kThr) sq[t] = t < len ? seg_of(p, f, bi, (long long)t0 + t) : -1;
   if (tid < p.Q) {
@@ -191,17 +187,13 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
     dtq[tid] = f.dte[bh0 * p.Lp + t0 + tid];
   }
   zero_padding(T, sXb, sYb, sB, sC, tid);  // B and C are contracted over tokens here
-  if (tid == 0) {
-    for (int k = 4; k < 9; ++k) mbar_init(&bar[k], 1);
-    mbar_fence_init();
-  }
   if (tid < 32) tmem_alloc(tmem_slot, 512);
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tmem_slot;
-  const uint32_t tDC = tm, tDB = tm + 128, tDM = tm + 256;
+  const uint32_t tDC = tm, tDB = tm + 128, tDM = tm + 256;  // dM buffers at 256 and 384
   bool ok = true;
 
   if (ctl) {
@@ -216,8 +208,9 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       auto issue_dm = [&](int hh) {  // dM = dy x^T of head hh (M = i, N = j, K = headdim)
         const int buf = hh & 1;
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tDM, kdesc_tok(sYb + buf * kTok, ks), kdesc_tok(sXb + buf * kTok, ks), id128, ks > 0);
-        mma_commit(b_dm);
+          mma_bf16(tDM + buf * 128, kdesc_tok(sYb + buf * kTok, ks), kdesc_tok(sXb + buf * kTok, ks), id128,
+                   ks > 0);
+        mma_commit(&b_dm[buf]);
       };
       if (!mbar_wait(&b_xy[0], 0)) ok = false;
       tc_fence_after();
@@ -226,38 +219,45 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
         const int buf = hh & 1;
         const uint8_t* sX = sXb + buf * kTok;
         const uint8_t* sY = sYb + buf * kTok;
+        const uint8_t* sS = sSb + buf * T.sbytes;
+        const uint8_t* sH = sHb + buf * T.sbytes;
+        // dM of the next head first, into the buffer head hh-1 used (its
+        // pass is done before head hh is scaled): ready when head hh's pass ends
+        if (hh + 1 < hpg) {
+          if (hh >= 1 && !mbar_wait(&b_dcb[buf ^ 1], ((hh - 1) >> 1) & 1)) ok = false;
+          if (!mbar_wait(&b_xy[buf ^ 1], ((hh + 1) >> 1) & 1)) ok = false;
+          tc_fence_after();
+          issue_dm(hh + 1);
+        }
         // carry and state: dC += (scaled dy) H, dB += (scaled x) dS  (K = headdim)
-        if (!mbar_wait(b_sc, hh & 1)) ok = false;  // x, dy of head hh scaled in place
-        if (!mbar_wait(b_sh, hh & 1)) ok = false;  // dS, H of head hh
+        if (!mbar_wait(&b_sc[buf], (hh >> 1) & 1)) ok = false;  // x, dy of head hh scaled in place
+        if (!mbar_wait(&b_sh[buf], (hh >> 1) & 1)) ok = false;  // dS, H of head hh
         tc_fence_after();
         for (int ks = 0; ks < 4; ++ks) {
           mma_bf16(tDC, kdesc_tok(sY, ks), kdesc_tok(sH, ks), idNk, (hh > 0 || ks > 0) ? 1u : 0u);
           mma_bf16(tDB, kdesc_tok(sX, ks), kdesc_tok(sS, ks), idNk, (hh > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(b_cs);
-        if (!mbar_wait(b_dcb, hh & 1)) ok = false;  // dCB of head hh written; dM read back
-        tc_fence_after();
-        if (hh + 1 < hpg) {  // dM of the next head first: the dB/dC work hides it
-          if (!mbar_wait(&b_xy[buf ^ 1], ((hh + 1) >> 1) & 1)) ok = false;
-          tc_fence_after();
-          issue_dm(hh + 1);
-        }
-        if (hh == 0 && !mbar_wait(b_bc, 0)) ok = false;  // B, C
-        tc_fence_after();
-        // dC += dCB B (A K-major, K = j);  dB += dCB^T C (A MN-major, K = i)
-        for (int ks = 0; ks < kRows / 16; ++ks) {
-          const uint64_t ak = smem_desc(smem_u32(sA) + (ks / 4) * kTok + (ks % 4) * 32, 16, 1024, kSwz128);
-          const uint64_t am = smem_desc(smem_u32(sA) + ks * 16 * 128, kTok, 1024, kSwz128);
-          mma_bf16(tDC, ak, mndesc_c(sB, ks), idNmn, 1u);
-          mma_bf16(tDB, am, mndesc_c(sC, ks), idNa_mn, 1u);
-        }
-        mma_commit(b_dbc);
-        // the carry and state MMAs of this head are done long since: release
-        // dS, H and this head's x, dy buffer to the next loads
+        // once the carry and state MMAs of head hh are done, its x/dy and
+        // dS/H buffers take the copies of head hh + 2
         if (!mbar_wait(b_cs, hh & 1)) ok = false;
-        if (hh + 1 < hpg) issue_sh(hh + 1);
-        if (hh + 2 < hpg) issue_xy(hh + 2);
+        if (hh + 2 < hpg) {
+          issue_xy(hh + 2);
+          issue_sh(hh + 2);
+        }
       }
+      mbar_arrive(b_fre);
+      // dC += S B (A K-major, K = j);  dB += S^T C (A MN-major, K = i)
+      if (!mbar_wait(b_afin, 0)) ok = false;
+      if (!mbar_wait(b_bc, 0)) ok = false;
+      tc_fence_after();
+      for (int ks = 0; ks < kRows / 16; ++ks) {
+        const uint64_t ak = smem_desc(smem_u32(sA) + (ks / 4) * kTok + (ks % 4) * 32, 16, 1024, kSwz128);
+        const uint64_t am = smem_desc(smem_u32(sA) + ks * 16 * 128, kTok, 1024, kSwz128);
+        mma_bf16(tDC, ak, mndesc_c(sB, ks), idNmn, 1u);
+        mma_bf16(tDB, am, mndesc_c(sC, ks), idNa_mn, 1u);
+      }
+      mma_commit(b_fin);
     }
   } else {
     // ---------------- 16 compute warps ----------------
@@ -268,7 +268,13 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
     const bool tok_ok = i < len;
     const int si = tok_ok ? sq[i] : -2;
     const int lim = tok_ok ? i : -1;
-    uint32_t ph_dm = 0, ph_dbc = 0;
+    // S = sum_h dCB^h for row i, columns 32 wg .. 32 wg + 31.  Blocks wholly
+    // above the diagonal block of the warp's 32 rows (wg > wq) stay zero.
+    float acc[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) acc[k] = 0.0f;
+    const int j0 = wg * 32;
+    const bool active = wg <= wq && j0 < len && wlane < len;  // warp-uniform
     for (int hh = 0; hh < hpg; ++hh) {
       const int buf = hh & 1;
       uint8_t* sX = sXb + buf * kTok;
@@ -282,15 +288,14 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       }
       cp_async_commit();
       // factor table of this head (its scalars are visible since the last
-      // barrier of the previous head, whose mask pass is done with the table);
-      // the barrier after the row scaling orders it before this mask pass
-      if (tid < 3 * p.Q) {
-        const int rb = 1 + tid / p.Q, j = tid % p.Q;
-        sfac[tid] = (j < 32 * rb && j < len) ? __expf(lb[32 * rb] - lb[j]) * db[j] : 0.0f;
+      // barrier of the previous head, whose pass is done with the table);
+      // the barrier after the row scaling orders it before this head's pass
+      if (tid < 4 * p.Q) {
+        const int rb = tid / p.Q, j = tid % p.Q;
+        sfac[tid] = (j < 32 * rb + 32 && j < len) ? __expf(lb[32 * rb] - lb[j]) * db[j] : 0.0f;
       }
       if (!mbar_wait(&b_xy[buf], (hh >> 1) & 1)) ok = false;  // x, dy of head hh
-      if (!mbar_wait(b_dm, ph_dm)) ok = false;                // dM of head hh has read them
-      ph_dm ^= 1;
+      if (!mbar_wait(&b_dm[buf], (hh >> 1) & 1)) ok = false;  // dM of head hh has read them
       tc_fence_after();
       // row scaling in place: warpgroups 0, 1 -> cv e^{l} dy (rows i), 2, 3 -> u x (rows j)
       {
@@ -322,73 +327,81 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       }
       fence_async_smem();
       named_sync_compute();
-      if (tid == 0) mbar_arrive(b_sc);
-      // dCB = dM o E o dt (row i, columns 32 wg .. 32 wg + 31); the dB/dC MMAs
-      // of head hh-1 must have read the previous dCB tile first
-      if (hh > 0) {
-        if (!mbar_wait(b_dbc, ph_dbc)) ok = false;
-        ph_dbc ^= 1;
-        tc_fence_after();
-      }
-      {
-        // units strictly below the diagonal block of the warp's 32 rows (one
-        // sequence in the chunk, A_h <= 0): exp(l_i - l_r) exp(l_r - l_j) dt_j
-        // with l_r the l of the block's first row, both factors <= 1, the
-        // second from the table; the others take the exact exponential
-        const bool fact = one_seg && f.A[h_first + hh] <= 0.0f;
+      if (tid == 0) mbar_arrive(&b_sc[buf]);
+      // S += dM o E o dt.  With one sequence in the chunk and A_h <= 0, l is
+      // non-increasing and the decay factors as exp(l_i - l_r) exp(l_r - l_j) dt_j,
+      // l_r the l of the warp's first row r: the first factor lies in (0, 1],
+      // the second comes from the table (<= dt_j left of the diagonal block;
+      // inside it <= e^60 dt_j, taken only where l drops by at most 60 over
+      // the block, so that neither factor leaves the fp32 range).  Every
+      // other case takes the exact exponential.
+      if (active) {
         const float li = tok_ok ? lb[i] : 0.0f;
-        const float r_row = wq > 0 ? __expf((tok_ok ? li : lb[len - 1]) - lb[32 * wq]) : 0.0f;
-        for (int q = wg * 2; q < wg * 2 + 2; ++q) {
-          const int j0 = q * 16;
-          uint32_t pk[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-          if (j0 <= wlane + 31 && j0 < len && fact && q < 2 * wq) {  // warp-uniform
-            float dm[16];
-            tmem_ld16(tmem_addr(tDM, wlane, j0), dm);
-            const float* sf = sfac + (wq - 1) * p.Q;
+        const int rl = min(wlane + 31, len - 1);
+        const bool fact = one_seg && f.A[h_first + hh] <= 0.0f && (wg < wq || lb[wlane] - lb[rl] <= 60.0f);
+        const float r_row = fact ? __expf((tok_ok ? li : lb[len - 1]) - lb[wlane]) : 0.0f;
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          const int jb = j0 + 16 * qq;
+          float* a = acc + 16 * qq;
+          float dm[16];
+          tmem_ld16(tmem_addr(tDM + buf * 128, wlane, jb), dm);
+          if (fact) {
+            const float* sf = sfac + wq * p.Q + jb;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const float4 sj = *reinterpret_cast<const float4*>(sf + j0 + 4 * k);
-              pk[2 * k] = pack2(dm[4 * k] * sj.x * r_row, dm[4 * k + 1] * sj.y * r_row);
-              pk[2 * k + 1] = pack2(dm[4 * k + 2] * sj.z * r_row, dm[4 * k + 3] * sj.w * r_row);
+              const float4 sj = *reinterpret_cast<const float4*>(sf + 4 * k);
+              const float sv[4] = {sj.x, sj.y, sj.z, sj.w};
+#pragma unroll
+              for (int m = 0; m < 4; ++m)
+                a[4 * k + m] = fmaf(dm[4 * k + m] * sv[m], jb + 4 * k + m <= lim ? r_row : 0.0f, a[4 * k + m]);
             }
-          } else if (j0 <= wlane + 31 && j0 < len) {  // warp-uniform; else every entry is masked
-            float dm[16];
-            tmem_ld16(tmem_addr(tDM, wlane, j0), dm);
+          } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const float4 lj = *reinterpret_cast<const float4*>(lb + j0 + 4 * k);
-              const float4 dj = *reinterpret_cast<const float4*>(db + j0 + 4 * k);
+              const float4 lj = *reinterpret_cast<const float4*>(lb + jb + 4 * k);
+              const float4 dj = *reinterpret_cast<const float4*>(db + jb + 4 * k);
               int4 sj = make_int4(si, si, si, si);
-              if (!one_seg) sj = *reinterpret_cast<const int4*>(sq + j0 + 4 * k);
+              if (!one_seg) sj = *reinterpret_cast<const int4*>(sq + jb + 4 * k);
               const float lv[4] = {lj.x, lj.y, lj.z, lj.w}, dv[4] = {dj.x, dj.y, dj.z, dj.w};
               const int sv[4] = {sj.x, sj.y, sj.z, sj.w};
-              float a4[4];
 #pragma unroll
               for (int m = 0; m < 4; ++m) {
-                const bool on = j0 + 4 * k + m <= lim && sv[m] == si;
-                a4[m] = dm[4 * k + m] * __expf(on ? li - lv[m] : -INFINITY) * dv[m];
+                const bool on = jb + 4 * k + m <= lim && sv[m] == si;
+                a[4 * k + m] = fmaf(dm[4 * k + m] * __expf(on ? li - lv[m] : -INFINITY), dv[m], a[4 * k + m]);
               }
-              pk[2 * k] = pack2(a4[0], a4[1]);
-              pk[2 * k + 1] = pack2(a4[2], a4[3]);
             }
           }
-          uint8_t* blk = sA + (q / 4) * kTok;
-          const uint32_t e0 = (q % 4) * 16;
-          *reinterpret_cast<uint4*>(blk + swz128_off(i, e0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(blk + swz128_off(i, e0 + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
       }
       cp_async_wait_all();  // this thread's scalar copies of head hh+1 have landed
-      fence_async_smem();
       tc_fence_before();
-      named_sync_compute();  // dCB complete; dM read back; the other slot's scalars visible
-      if (tid == 0) mbar_arrive(b_dcb);
+      named_sync_compute();  // dM read back; the table free; the other slot's scalars visible
+      if (tid == 0) mbar_arrive(&b_dcb[buf]);
     }
-    if (!mbar_wait(b_dbc, ph_dbc)) ok = false;  // the last head's dB/dC MMAs
+    // S as a bf16 tile (rows i, K-major over j) in the x tiles, once every
+    // head's copies have been consumed
+    if (!mbar_wait(b_fre, 0)) ok = false;
+    {
+      uint8_t* blk = sA + (wg >> 1) * kTok;
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        const uint32_t e0 = (wg & 1) * 32 + qq * 16;
+        const float* a = acc + 16 * qq;
+        *reinterpret_cast<uint4*>(blk + swz128_off(i, e0)) =
+            make_uint4(pack2(a[0], a[1]), pack2(a[2], a[3]), pack2(a[4], a[5]), pack2(a[6], a[7]));
+        *reinterpret_cast<uint4*>(blk + swz128_off(i, e0 + 8)) =
+            make_uint4(pack2(a[8], a[9]), pack2(a[10], a[11]), pack2(a[12], a[13]), pack2(a[14], a[15]));
+      }
+    }
+    fence_async_smem();
+    named_sync_compute();
+    if (tid == 0) mbar_arrive(b_afin);
+    if (!mbar_wait(b_fin, 0)) ok = false;  // the final dB/dC MMAs
     tc_fence_after();
     // epilogue: rows of dB and dC (thread = token t; d_state columns 16 q, q = wg mod 4).
     // With 128-byte rows (d_state >= 64) they are staged in the x and dy
-    // tiles, free once the last head's products are done, in the layout of a
+    // tiles, free once the final products are done, in the layout of a
     // tensor copy, and leave by tensor stores (rows past the sequence are
     // clipped); narrower states take plain stores.
     {
@@ -407,7 +420,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
         const uint4 c0 = make_uint4(pack2(vc[0], vc[1]), pack2(vc[2], vc[3]), pack2(vc[4], vc[5]), pack2(vc[6], vc[7]));
         const uint4 c1 = make_uint4(pack2(vc[8], vc[9]), pack2(vc[10], vc[11]), pack2(vc[12], vc[13]), pack2(vc[14], vc[15]));
         if (staged) {
-          uint8_t* sb = sXb + (q >> 2) * kTok;          // dB column block q / 4
+          uint8_t* sb = sXb + (q >> 2) * kTok;            // dB column block q / 4
           uint8_t* sc = sXb + (T.ncb + (q >> 2)) * kTok;  // dC column block q / 4
           const uint32_t e0 = (q & 3) * 16;
           *reinterpret_cast<uint4*>(sb + swz128_off(t, e0)) = b0;
@@ -476,7 +489,7 @@ cudaError_t launch_chunk_bwd_dbc_group_tc(const Plan& p, const Bufs& f, cudaStre
   const GTiles T = gtiles(p.N, p.Q);
   CUtensorMap X, Y, B, C, S, H, DB, DC;
   if (!group_maps(p, f, &X, &Y, &B, &C, &S, &H, &DB, &DC)) return cudaErrorInvalidValue;
-  const size_t smem = group_smem_bytes(T, p.Q, p.hpg);
+  const size_t smem = group_smem_bytes(T, p.Q);
   cudaError_t e = cudaFuncSetAttribute(chunk_bwd_dbc_group_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

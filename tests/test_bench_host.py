@@ -126,10 +126,11 @@ def test_kernel_model_flops_match_a_hand_count():
     cb = 2 * 128 * 128 * 32
     per_head = 2 * 128 * 128 * 64 + 2 * (2 * 128 * 64 * 32) + 2 * 128 * 64 * 128
     assert m["chunk_bwd"]["flops"] == cb + 2 * per_head == 11534336
-    # dB/dC kernel, per head: dy x^T, dy H and x dS (128x32x64 each),
-    # dCB B and dCB^T C (128x32x128 each)
-    per_head = 2 * 128 * 128 * 64 + 2 * (2 * 128 * 32 * 64) + 2 * (2 * 128 * 32 * 128)
-    assert m["chunk_bwd_dbc"]["flops"] == 2 * per_head == 10485760
+    # dB/dC kernel, per head: dy x^T, dy H and x dS (128x32x64 each); once
+    # per group, on the heads' summed dCB: S B and S^T C (128x32x128 each)
+    per_head = 2 * 128 * 128 * 64 + 2 * (2 * 128 * 32 * 64)
+    per_group = 2 * (2 * 128 * 32 * 128)
+    assert m["chunk_bwd_dbc"]["flops"] == 2 * per_head + per_group == 8388608
     # chunk_scan at chunk 128: C B^T and C_rev B^T once, per head A_hat X
     # (128x64x128) and C H^T (128x64x32)
     assert m["chunk_scan"]["flops"] == 2 * cb + 2 * (2 * 128 * 64 * 128 + 2 * 128 * 64 * 32)
