@@ -46,13 +46,15 @@ __host__ __device__ inline uint32_t r1024(uint32_t v) { return (v + 1023u) & ~10
 
 struct GTiles {
   int rows, cw, ncb;
+  bool aliasA;
   uint32_t cblk, cswz, cbytes, sbytes;
-  uint32_t offB, offC, offX, offY, offS, offH, offF;
+  uint32_t offB, offC, offX, offY, offS, offH, offA, offF;
 };
 
 // Shared memory: B, C (the final products), x[2], dy[2] (contiguous: the
-// S tile and the dB/dC staging reuse them once every head is done), dS[2],
-// H[2], then the scalars.
+// dB/dC staging reuses them once every head is done), dS[2], H[2], the
+// bf16 S tile (at d_state 128 it shares the dS/H buffers that the last two
+// heads leave free), then the scalars.
 __host__ __device__ inline GTiles gtiles(int N, int Q) {
   GTiles t;
   t.rows = Q < kRows ? Q : kRows;
@@ -68,16 +70,21 @@ __host__ __device__ inline GTiles gtiles(int N, int Q) {
   t.offY = t.offX + 2 * kTok;
   t.offS = t.offY + 2 * kTok;
   t.offH = t.offS + 2 * t.sbytes;
-  t.offF = t.offH + 2 * t.sbytes;
+  t.aliasA = t.sbytes >= kTok;
+  t.offA = t.offH + 2 * t.sbytes;
+  t.offF = t.aliasA ? t.offA : t.offA + 2 * kTok;
   return t;
 }
 
-constexpr int kBars = 15;
+constexpr int kCw = kCompute / 32;  // compute warps: one arrival each on the per-head barriers
+constexpr int kMaxHpg = 256;
+constexpr int kBars = 19;
 
-// Scalars after the tiles: l and dt of two heads, the segment ids, the
-// factor table; then the barriers and the tensor-memory address.
+// Scalars after the tiles: l and dt of four heads (a ring filled by bulk
+// copies), the segment ids, a 32-entry factor table per warp, A of the
+// group's heads; then the barriers and the tensor-memory address.
 __host__ __device__ inline size_t group_smem_bytes(const GTiles& T, int Q) {
-  return 1024 + T.offF + (size_t)9 * Q * 4 + kBars * 8 + 16;
+  return 1024 + T.offF + (size_t)(8 * Q + Q + kCw * 32 + kMaxHpg) * 4 + kBars * 8 + 16;
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -123,33 +130,39 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const GTiles T = gtiles(p.N, p.Q);
+  const int hpg = p.hpg;
   uint8_t* sB = sm + T.offB;
   uint8_t* sC = sm + T.offC;
   uint8_t* sXb = sm + T.offX;
   uint8_t* sYb = sm + T.offY;
   uint8_t* sSb = sm + T.offS;
   uint8_t* sHb = sm + T.offH;
-  uint8_t* sA = sXb;  // the S tile, once the heads are done (two 64-column blocks)
-  float* lq = reinterpret_cast<float*>(sm + T.offF);  // [2 slots][Q]
-  float* dtq = lq + 2 * p.Q;                          // [2 slots][Q]
-  int* sq = reinterpret_cast<int*>(dtq + 2 * p.Q);    // [Q]
-  float* sfac = reinterpret_cast<float*>(sq + p.Q);   // [4][Q] exp(l_{32 rb} - l_j) dt_j, j < 32 rb + 32
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sfac + 4 * p.Q);
+  // the S tile's two 64-column blocks: at d_state 128 in the dS and H
+  // buffers of parity hpg & 1 (no head after hpg - 3 is loaded there)
+  uint8_t* sA0 = T.aliasA ? sSb + (hpg & 1) * T.sbytes : sm + T.offA;
+  uint8_t* sA1 = T.aliasA ? sHb + (hpg & 1) * T.sbytes : sm + T.offA + kTok;
+  float* lsl = reinterpret_cast<float*>(sm + T.offF);  // [4 slots][l, dt][Q]
+  int* sq = reinterpret_cast<int*>(lsl + 8 * p.Q);     // [Q]
+  float* wtab = reinterpret_cast<float*>(sq + p.Q);    // [warp][32] exp(l_r - l_j) dt_j
+  float* Ah = wtab + kCw * 32;                         // [kMaxHpg]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(Ah + kMaxHpg);
   // bc: B, C loaded; xy[2], sh[2]: x/dy and dS/H buffers loaded; dm[2]: dM
-  // in tensor-memory buffer k done; sc[2]: x, dy in buffer k scaled in
-  // place; cs: carry/state MMAs done; dcb[2]: dM buffer k read back; fre:
-  // every head's copies consumed; afin: S tile written; fin: final MMAs done
+  // in tensor-memory buffer k done; sc[2]: every warp has scaled its part of
+  // the x, dy buffer k; cs: carry/state MMAs done; dcb[2]: every warp is done
+  // with the head of dM buffer k (its dM, its scalars); fre: the S tile's
+  // buffers hold no further head; afin: S tile written; fin: final MMAs
+  // done; lq[4]: scalars of the head in ring slot k loaded
   uint64_t *b_bc = bar, *b_xy = bar + 1, *b_sh = bar + 3, *b_dm = bar + 5, *b_sc = bar + 7, *b_cs = bar + 9,
-           *b_dcb = bar + 10, *b_fre = bar + 12, *b_afin = bar + 13, *b_fin = bar + 14;
+           *b_dcb = bar + 10, *b_fre = bar + 12, *b_afin = bar + 13, *b_fin = bar + 14, *b_lq = bar + 15;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kBars);
 
   const int c = blockIdx.x, g = blockIdx.y, bi = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool ctl = tid >= kCompute;
   const int wg = (tid >> 7) & 3, r = tid & 127, wq = (tid >> 5) & 3;
   const int wlane = wq * 32;
   const int t0 = c * p.Q, len = min(p.Q, p.L - t0);
-  const int hpg = p.hpg, h_first = g * hpg;
+  const int h_first = g * hpg;
   const long long bh0 = (long long)bi * p.H + h_first;
   const uint32_t tok_bytes = (uint32_t)T.rows * 128u;
   const uint32_t c_bytes = (uint32_t)T.ncb * T.rows * T.cw;
@@ -166,14 +179,29 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
     tma_load_4d(sSb + buf * T.sbytes, &tmS, &b_sh[buf], 0, 0, c, bi * p.H + h);
     tma_load_4d(sHb + buf * T.sbytes, &tmH, &b_sh[buf], 0, 0, c, bi * p.H + h);
   };
-  if (tid == kCompute) {  // the control lane starts the tile copies first
-    for (int k = 0; k < kBars; ++k) mbar_init(&bar[k], 1);
+  auto issue_lq = [&](int hh) {  // l and dt of head hh (Q floats each, 16-byte aligned) into slot hh % 4
+    const int s = hh & 3;
+    const long long o = (bh0 + hh) * p.Lp + t0;
+    mbar_expect_tx(&b_lq[s], 2 * p.Q * 4);
+    bulk_load(lsl + s * 2 * p.Q, f.lcs + o, p.Q * 4, &b_lq[s]);
+    bulk_load(lsl + s * 2 * p.Q + p.Q, f.dte + o, p.Q * 4, &b_lq[s]);
+  };
+  if (tid == kCompute) {  // the control lane starts the copies first
+    for (int k = 0; k < kBars; ++k) {
+      const bool per_warp = bar + k == b_sc || bar + k == b_sc + 1 || bar + k == b_dcb || bar + k == b_dcb + 1 ||
+                            bar + k == b_afin;
+      mbar_init(&bar[k], per_warp ? kCw : 1);
+    }
     mbar_fence_init();
+    issue_lq(0);
     issue_xy(0);
     issue_sh(0);
-    if (hpg > 1) {
-      issue_xy(1);
-      issue_sh(1);
+    for (int hh = 1; hh < 3 && hh < hpg; ++hh) {
+      issue_lq(hh);
+      if (hh < 2) {
+        issue_xy(hh);
+        issue_sh(hh);
+      }
     }
     mbar_expect_tx(b_bc, 2 * c_bytes);
     for (int q = 0; q < T.ncb; ++q) {
@@ -182,10 +210,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
     }
   }
   for (int t = tid; t < p.Q; t += kThr) sq[t] = t < len ? seg_of(p, f, bi, (long long)t0 + t) : -1;
-  if (tid < p.Q) {
-    lq[tid] = f.lcs[bh0 * p.Lp + t0 + tid];
-    dtq[tid] = f.dte[bh0 * p.Lp + t0 + tid];
-  }
+  for (int k = tid; k < hpg; k += kThr) Ah[k] = f.A[h_first + k];
   zero_padding(T, sXb, sYb, sB, sC, tid);  // B and C are contracted over tokens here
   if (tid < 32) tmem_alloc(tmem_slot, 512);
   fence_async_smem();
@@ -215,16 +240,18 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       if (!mbar_wait(&b_xy[0], 0)) ok = false;
       tc_fence_after();
       issue_dm(0);
+      if (hpg == 1) mbar_arrive(b_fre);  // the parity-1 buffers are never used
       for (int hh = 0; hh < hpg; ++hh) {
         const int buf = hh & 1;
         const uint8_t* sX = sXb + buf * kTok;
         const uint8_t* sY = sYb + buf * kTok;
         const uint8_t* sS = sSb + buf * T.sbytes;
         const uint8_t* sH = sHb + buf * T.sbytes;
-        // dM of the next head first, into the buffer head hh-1 used (its
-        // pass is done before head hh is scaled): ready when head hh's pass ends
+        // every warp is done with head hh-1: its dM buffer takes the next
+        // head's dM, its scalar slot the scalars of head hh+3
+        if (hh >= 1 && hh + 1 < hpg && !mbar_wait(&b_dcb[buf ^ 1], ((hh - 1) >> 1) & 1)) ok = false;
+        if (hh + 3 < hpg) issue_lq(hh + 3);
         if (hh + 1 < hpg) {
-          if (hh >= 1 && !mbar_wait(&b_dcb[buf ^ 1], ((hh - 1) >> 1) & 1)) ok = false;
           if (!mbar_wait(&b_xy[buf ^ 1], ((hh + 1) >> 1) & 1)) ok = false;
           tc_fence_after();
           issue_dm(hh + 1);
@@ -245,22 +272,23 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
           issue_xy(hh + 2);
           issue_sh(hh + 2);
         }
+        if (hh + 2 == hpg) mbar_arrive(b_fre);  // parity hpg & 1 holds no further head
       }
-      mbar_arrive(b_fre);
       // dC += S B (A K-major, K = j);  dB += S^T C (A MN-major, K = i)
       if (!mbar_wait(b_afin, 0)) ok = false;
       if (!mbar_wait(b_bc, 0)) ok = false;
       tc_fence_after();
+      const uint32_t a0 = smem_u32(sA0), lbo = smem_u32(sA1) - a0;
       for (int ks = 0; ks < kRows / 16; ++ks) {
-        const uint64_t ak = smem_desc(smem_u32(sA) + (ks / 4) * kTok + (ks % 4) * 32, 16, 1024, kSwz128);
-        const uint64_t am = smem_desc(smem_u32(sA) + ks * 16 * 128, kTok, 1024, kSwz128);
+        const uint64_t ak = smem_desc((ks < 4 ? a0 : a0 + lbo) + (ks % 4) * 32, 16, 1024, kSwz128);
+        const uint64_t am = smem_desc(a0 + ks * 16 * 128, lbo, 1024, kSwz128);
         mma_bf16(tDC, ak, mndesc_c(sB, ks), idNmn, 1u);
         mma_bf16(tDB, am, mndesc_c(sC, ks), idNa_mn, 1u);
       }
       mma_commit(b_fin);
     }
   } else {
-    // ---------------- 16 compute warps ----------------
+    // ---------------- 16 compute warps, each on its own ----------------
     const int s_in = seg_in_of(p, f, bi, c);
     const int s_last = sq[len - 1];
     const bool one_seg = sq[0] == s_last;
@@ -268,6 +296,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
     const bool tok_ok = i < len;
     const int si = tok_ok ? sq[i] : -2;
     const int lim = tok_ok ? i : -1;
+    float* tab = wtab + warp * 32;
     // S = sum_h dCB^h for row i, columns 32 wg .. 32 wg + 31.  Blocks wholly
     // above the diagonal block of the warp's 32 rows (wg > wq) stay zero.
     float acc[32];
@@ -279,25 +308,14 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       const int buf = hh & 1;
       uint8_t* sX = sXb + buf * kTok;
       uint8_t* sY = sYb + buf * kTok;
-      const float* lb = lq + buf * p.Q;
-      const float* db = dtq + buf * p.Q;
-      if (hh + 1 < hpg && tid < p.Q) {  // scalars of head hh+1 into the other slot
-        const long long bhn = bh0 + hh + 1;
-        cp_async4(lq + (buf ^ 1) * p.Q + tid, f.lcs + bhn * p.Lp + t0 + tid);
-        cp_async4(dtq + (buf ^ 1) * p.Q + tid, f.dte + bhn * p.Lp + t0 + tid);
-      }
-      cp_async_commit();
-      // factor table of this head (its scalars are visible since the last
-      // barrier of the previous head, whose pass is done with the table);
-      // the barrier after the row scaling orders it before this head's pass
-      if (tid < 4 * p.Q) {
-        const int rb = tid / p.Q, j = tid % p.Q;
-        sfac[tid] = (j < 32 * rb + 32 && j < len) ? __expf(lb[32 * rb] - lb[j]) * db[j] : 0.0f;
-      }
-      if (!mbar_wait(&b_xy[buf], (hh >> 1) & 1)) ok = false;  // x, dy of head hh
-      if (!mbar_wait(&b_dm[buf], (hh >> 1) & 1)) ok = false;  // dM of head hh has read them
+      const float* lb = lsl + (hh & 3) * 2 * p.Q;
+      const float* db = lb + p.Q;
+      if (!mbar_wait(&b_lq[hh & 3], (hh >> 2) & 1)) ok = false;  // l, dt of head hh
+      if (!mbar_wait(&b_xy[buf], (hh >> 1) & 1)) ok = false;     // x, dy of head hh
+      if (!mbar_wait(&b_dm[buf], (hh >> 1) & 1)) ok = false;     // dM of head hh has read them
       tc_fence_after();
-      // row scaling in place: warpgroups 0, 1 -> cv e^{l} dy (rows i), 2, 3 -> u x (rows j)
+      // row scaling in place, 32 rows x 32 columns per warp: warpgroups 0, 1
+      // -> cv e^{l} dy (rows i), 2, 3 -> u x (rows j)
       {
         const int t = r;
         const bool v = t < len;
@@ -326,20 +344,26 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
         }
       }
       fence_async_smem();
-      named_sync_compute();
-      if (tid == 0) mbar_arrive(&b_sc[buf]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b_sc[buf]);
       // S += dM o E o dt.  With one sequence in the chunk and A_h <= 0, l is
       // non-increasing and the decay factors as exp(l_i - l_r) exp(l_r - l_j) dt_j,
       // l_r the l of the warp's first row r: the first factor lies in (0, 1],
-      // the second comes from the table (<= dt_j left of the diagonal block;
-      // inside it <= e^60 dt_j, taken only where l drops by at most 60 over
-      // the block, so that neither factor leaves the fp32 range).  Every
+      // the second comes from the warp's table (<= dt_j left of the diagonal
+      // block; inside it <= e^60 dt_j, taken only where l drops by at most 60
+      // over the block, so that neither factor leaves the fp32 range).  Every
       // other case takes the exact exponential.
       if (active) {
         const float li = tok_ok ? lb[i] : 0.0f;
         const int rl = min(wlane + 31, len - 1);
-        const bool fact = one_seg && f.A[h_first + hh] <= 0.0f && (wg < wq || lb[wlane] - lb[rl] <= 60.0f);
-        const float r_row = fact ? __expf((tok_ok ? li : lb[len - 1]) - lb[wlane]) : 0.0f;
+        const bool fact = one_seg && Ah[hh] <= 0.0f && (wg < wq || lb[wlane] - lb[rl] <= 60.0f);
+        float r_row = 0.0f;
+        if (fact) {
+          const int j = j0 + lane;
+          tab[lane] = j < len ? __expf(lb[wlane] - lb[j]) * db[j] : 0.0f;
+          r_row = __expf((tok_ok ? li : lb[len - 1]) - lb[wlane]);
+          __syncwarp();
+        }
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
           const int jb = j0 + 16 * qq;
@@ -347,7 +371,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
           float dm[16];
           tmem_ld16(tmem_addr(tDM + buf * 128, wlane, jb), dm);
           if (fact) {
-            const float* sf = sfac + wq * p.Q + jb;
+            const float* sf = tab + 16 * qq;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const float4 sj = *reinterpret_cast<const float4*>(sf + 4 * k);
@@ -374,16 +398,14 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
           }
         }
       }
-      cp_async_wait_all();  // this thread's scalar copies of head hh+1 have landed
       tc_fence_before();
-      named_sync_compute();  // dM read back; the table free; the other slot's scalars visible
-      if (tid == 0) mbar_arrive(&b_dcb[buf]);
+      __syncwarp();  // the warp is done with this head's dM, scalars and table
+      if (lane == 0) mbar_arrive(&b_dcb[buf]);
     }
-    // S as a bf16 tile (rows i, K-major over j) in the x tiles, once every
-    // head's copies have been consumed
+    // S as a bf16 tile (rows i, K-major over j), once its buffers are free
     if (!mbar_wait(b_fre, 0)) ok = false;
     {
-      uint8_t* blk = sA + (wg >> 1) * kTok;
+      uint8_t* blk = (wg >> 1) ? sA1 : sA0;
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const uint32_t e0 = (wg & 1) * 32 + qq * 16;
@@ -395,8 +417,8 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       }
     }
     fence_async_smem();
-    named_sync_compute();
-    if (tid == 0) mbar_arrive(b_afin);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b_afin);
     if (!mbar_wait(b_fin, 0)) ok = false;  // the final dB/dC MMAs
     tc_fence_after();
     // epilogue: rows of dB and dC (thread = token t; d_state columns 16 q, q = wg mod 4).
