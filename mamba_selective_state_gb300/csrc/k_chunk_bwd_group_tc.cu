@@ -41,34 +41,32 @@ constexpr int kRows = 128;
 constexpr int kCompute = 512;        // 16 compute warps: four read each quarter of the TMEM lanes
 constexpr int kThr = kCompute + 32;  // and one control warp for the copies and MMAs
 constexpr uint32_t kTok = kRows * 128u;  // one (128 tokens x 64) bf16 tile
+constexpr uint32_t kSlot = 2 * kTok;       // an x tile and a dy tile
 
 __host__ __device__ inline uint32_t r1024(uint32_t v) { return (v + 1023u) & ~1023u; }
 
 struct GTiles {
-  int rows, cw, ncb;
+  int cw, ncb;
   bool aliasA;
   uint32_t cblk, cswz, cbytes, sbytes;
-  uint32_t offB, offC, offX, offY, offS, offH, offA, offF;
+  uint32_t offX, offS, offH, offA, offF;
 };
 
-// Shared memory: B, C (the final products), x[2], dy[2] (contiguous: the
-// dB/dC staging reuses them once every head is done), dS[2], H[2], the
-// bf16 S tile (at d_state 128 it shares the dS/H buffers that the last two
-// heads leave free), then the scalars.
-__host__ __device__ inline GTiles gtiles(int N, int Q) {
+// Shared memory: three (x, dy) slots, each x then dy (slots 0 and 1 also
+// stage the dB/dC rows at the end), dS[2], H[2], the bf16 S tile (at
+// d_state 128 in the dS/H buffers that the last two heads leave free), then
+// the scalars.  B and C are only needed by the two final products: they
+// arrive in the x/dy slots that the last heads leave free.
+__host__ __device__ inline GTiles gtiles(int N) {
   GTiles t;
-  t.rows = Q < kRows ? Q : kRows;
   t.cw = 2 * (N < 64 ? N : 64);
   t.ncb = N >= 64 ? N / 64 : 1;
   t.cblk = (uint32_t)kRows * t.cw;
   t.cswz = t.cw == 128 ? kSwz128 : (t.cw == 64 ? kSwz64 : kSwz32);
-  t.cbytes = r1024(t.ncb * t.cblk);
+  t.cbytes = r1024(t.ncb * t.cblk);  // <= 2 kTok: B or C fits one x/dy slot
   t.sbytes = r1024((uint32_t)N * 128u);
-  t.offB = 0;
-  t.offC = t.cbytes;
-  t.offX = 2 * t.cbytes;
-  t.offY = t.offX + 2 * kTok;
-  t.offS = t.offY + 2 * kTok;
+  t.offX = 0;
+  t.offS = t.offX + 3 * kSlot;
   t.offH = t.offS + 2 * t.sbytes;
   t.aliasA = t.sbytes >= kTok;
   t.offA = t.offH + 2 * t.sbytes;
@@ -78,13 +76,13 @@ __host__ __device__ inline GTiles gtiles(int N, int Q) {
 
 constexpr int kCw = kCompute / 32;  // compute warps: one arrival each on the per-head barriers
 constexpr int kMaxHpg = 256;
-constexpr int kBars = 19;
+constexpr int kBars = 22;
 
 // Scalars after the tiles: l and dt of four heads (a ring filled by bulk
 // copies), the segment ids, a 32-entry factor table per warp, A of the
 // group's heads; then the barriers and the tensor-memory address.
-__host__ __device__ inline size_t group_smem_bytes(const GTiles& T, int Q) {
-  return 1024 + T.offF + (size_t)(8 * Q + Q + kCw * 32 + kMaxHpg) * 4 + kBars * 8 + 16;
+__host__ __device__ inline size_t group_smem_bytes(const GTiles& T) {
+  return 1024 + T.offF + (size_t)(9 * kRows + kCw * 32 + kMaxHpg) * 4 + kBars * 8 + 16;
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -93,25 +91,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 }
 __device__ __forceinline__ float2 unpack2(uint32_t v) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
-}
-
-// Rows beyond a short chunk (chunk < 128) of the x, dy, B and C tiles are
-// never written by the tensor copies: zero them once, so that they add
-// exact zeros wherever a contraction runs over tokens.
-__device__ __forceinline__ void zero_padding(const GTiles& T, uint8_t* sXb, uint8_t* sYb, uint8_t* sB,
-                                             uint8_t* sC, int tid) {
-  if (T.rows >= kRows) return;
-  for (int idx = tid; idx < 4 * (kRows - T.rows) * 8; idx += blockDim.x) {
-    const int which = idx / ((kRows - T.rows) * 8), k = idx % ((kRows - T.rows) * 8);
-    uint8_t* base = (which < 2 ? sXb : sYb) + (which & 1) * kTok + T.rows * 128;
-    reinterpret_cast<uint4*>(base)[k] = make_uint4(0, 0, 0, 0);
-  }
-  const int per = (kRows - T.rows) * T.cw / 16;
-  for (int idx = tid; idx < 2 * T.ncb * per; idx += blockDim.x) {
-    const int blk = idx / per, k = idx % per;
-    uint8_t* base = (blk < T.ncb ? sB : sC) + (blk % T.ncb) * T.cblk + T.rows * T.cw;
-    reinterpret_cast<uint4*>(base)[k] = make_uint4(0, 0, 0, 0);
-  }
 }
 
 __device__ __forceinline__ void named_sync_compute() {  // the 16 compute warps only
@@ -129,31 +108,34 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
                                                                         const __grid_constant__ CUtensorMap tmDC) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const GTiles T = gtiles(p.N, p.Q);
+  const GTiles T = gtiles(p.N);
   const int hpg = p.hpg;
-  uint8_t* sB = sm + T.offB;
-  uint8_t* sC = sm + T.offC;
   uint8_t* sXb = sm + T.offX;
-  uint8_t* sYb = sm + T.offY;
   uint8_t* sSb = sm + T.offS;
   uint8_t* sHb = sm + T.offH;
+  auto sX = [&](int hh) { return sXb + (hh % 3) * kSlot; };
+  auto sY = [&](int hh) { return sXb + (hh % 3) * kSlot + kTok; };
+  // B in the slot of head hpg - 3, C in that of head hpg - 2 (neither holds a later head)
+  uint8_t* sB = sXb + (hpg % 3) * kSlot;
+  uint8_t* sC = sXb + ((hpg + 1) % 3) * kSlot;
   // the S tile's two 64-column blocks: at d_state 128 in the dS and H
-  // buffers of parity hpg & 1 (no head after hpg - 3 is loaded there)
+  // buffers of parity hpg & 1 (no head after hpg - 2 is loaded there)
   uint8_t* sA0 = T.aliasA ? sSb + (hpg & 1) * T.sbytes : sm + T.offA;
   uint8_t* sA1 = T.aliasA ? sHb + (hpg & 1) * T.sbytes : sm + T.offA + kTok;
   float* lsl = reinterpret_cast<float*>(sm + T.offF);  // [4 slots][l, dt][Q]
-  int* sq = reinterpret_cast<int*>(lsl + 8 * p.Q);     // [Q]
-  float* wtab = reinterpret_cast<float*>(sq + p.Q);    // [warp][32] exp(l_r - l_j) dt_j
+  int* sq = reinterpret_cast<int*>(lsl + 8 * kRows);   // [Q]
+  float* wtab = reinterpret_cast<float*>(sq + kRows);  // [warp][32] exp(l_r - l_j) dt_j
   float* Ah = wtab + kCw * 32;                         // [kMaxHpg]
   uint64_t* bar = reinterpret_cast<uint64_t*>(Ah + kMaxHpg);
-  // bc: B, C loaded; xy[2], sh[2]: x/dy and dS/H buffers loaded; dm[2]: dM
-  // in tensor-memory buffer k done; sc[2]: every warp has scaled its part of
-  // the x, dy buffer k; cs: carry/state MMAs done; dcb[2]: every warp is done
-  // with the head of dM buffer k (its dM, its scalars); fre: the S tile's
-  // buffers hold no further head; afin: S tile written; fin: final MMAs
-  // done; lq[4]: scalars of the head in ring slot k loaded
-  uint64_t *b_bc = bar, *b_xy = bar + 1, *b_sh = bar + 3, *b_dm = bar + 5, *b_sc = bar + 7, *b_cs = bar + 9,
-           *b_dcb = bar + 10, *b_fre = bar + 12, *b_afin = bar + 13, *b_fin = bar + 14, *b_lq = bar + 15;
+  // b, c: B, C loaded; xy[3], sh[2]: x/dy slots and dS/H buffers loaded;
+  // dm[2]: dM in tensor-memory buffer k done; sc[2]: every warp has scaled
+  // its part of the x, dy of head parity k; cs: carry/state MMAs done;
+  // dcb[2]: every warp is done with the head of dM buffer k (its dM, its
+  // scalars); fre: the S tile's buffers hold no further head; afin: S tile
+  // written; fin: final MMAs done; lq[4]: scalars of ring slot k loaded
+  uint64_t *b_b = bar, *b_c = bar + 1, *b_xy = bar + 2, *b_sh = bar + 5, *b_dm = bar + 7, *b_sc = bar + 9,
+           *b_cs = bar + 11, *b_dcb = bar + 12, *b_fre = bar + 14, *b_afin = bar + 15, *b_fin = bar + 16,
+           *b_lq = bar + 17;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kBars);
 
   const int c = blockIdx.x, g = blockIdx.y, bi = blockIdx.z;
@@ -161,17 +143,17 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
   const bool ctl = tid >= kCompute;
   const int wg = (tid >> 7) & 3, r = tid & 127, wq = (tid >> 5) & 3;
   const int wlane = wq * 32;
-  const int t0 = c * p.Q, len = min(p.Q, p.L - t0);
+  const int t0 = c * kRows, len = min(kRows, p.L - t0);
   const int h_first = g * hpg;
   const long long bh0 = (long long)bi * p.H + h_first;
-  const uint32_t tok_bytes = (uint32_t)T.rows * 128u;
-  const uint32_t c_bytes = (uint32_t)T.ncb * T.rows * T.cw;
+  const uint32_t c_bytes = (uint32_t)T.ncb * T.cblk;
   const uint32_t s_bytes = (uint32_t)p.N * 128u;
   auto issue_xy = [&](int hh) {
-    const int buf = hh & 1, h = h_first + hh;
-    mbar_expect_tx(&b_xy[buf], 2 * tok_bytes);
-    tma_load_4d(sXb + buf * kTok, &tmX, &b_xy[buf], 0, h, t0, bi);
-    tma_load_4d(sYb + buf * kTok, &tmY, &b_xy[buf], 0, h, t0, bi);
+    uint64_t* bb = &b_xy[hh % 3];
+    const int h = h_first + hh;
+    mbar_expect_tx(bb, 2 * kTok);
+    tma_load_4d(sX(hh), &tmX, bb, 0, h, t0, bi);
+    tma_load_4d(sY(hh), &tmY, bb, 0, h, t0, bi);
   };
   auto issue_sh = [&](int hh) {
     const int buf = hh & 1, h = h_first + hh;
@@ -182,9 +164,13 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
   auto issue_lq = [&](int hh) {  // l and dt of head hh (Q floats each, 16-byte aligned) into slot hh % 4
     const int s = hh & 3;
     const long long o = (bh0 + hh) * p.Lp + t0;
-    mbar_expect_tx(&b_lq[s], 2 * p.Q * 4);
-    bulk_load(lsl + s * 2 * p.Q, f.lcs + o, p.Q * 4, &b_lq[s]);
-    bulk_load(lsl + s * 2 * p.Q + p.Q, f.dte + o, p.Q * 4, &b_lq[s]);
+    mbar_expect_tx(&b_lq[s], 2 * kRows * 4);
+    bulk_load(lsl + s * 2 * kRows, f.lcs + o, kRows * 4, &b_lq[s]);
+    bulk_load(lsl + s * 2 * kRows + kRows, f.dte + o, kRows * 4, &b_lq[s]);
+  };
+  auto issue_bc = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bb) {
+    mbar_expect_tx(bb, c_bytes);
+    for (int q = 0; q < T.ncb; ++q) tma_load_4d(dst + q * T.cblk, map, bb, q * 64, g, t0, bi);
   };
   if (tid == kCompute) {  // the control lane starts the copies first
     for (int k = 0; k < kBars; ++k) {
@@ -193,27 +179,17 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       mbar_init(&bar[k], per_warp ? kCw : 1);
     }
     mbar_fence_init();
-    issue_lq(0);
-    issue_xy(0);
-    issue_sh(0);
-    for (int hh = 1; hh < 3 && hh < hpg; ++hh) {
+    for (int hh = 0; hh < 3 && hh < hpg; ++hh) {
       issue_lq(hh);
-      if (hh < 2) {
-        issue_xy(hh);
-        issue_sh(hh);
-      }
+      issue_xy(hh);
+      if (hh < 2) issue_sh(hh);
     }
-    mbar_expect_tx(b_bc, 2 * c_bytes);
-    for (int q = 0; q < T.ncb; ++q) {
-      tma_load_4d(sB + q * T.cblk, &tmB, b_bc, q * 64, g, t0, bi);
-      tma_load_4d(sC + q * T.cblk, &tmC, b_bc, q * 64, g, t0, bi);
-    }
+    if (hpg < 3) issue_bc(sB, &tmB, b_b);  // slots no head uses
+    if (hpg < 2) issue_bc(sC, &tmC, b_c);
   }
-  for (int t = tid; t < p.Q; t += kThr) sq[t] = t < len ? seg_of(p, f, bi, (long long)t0 + t) : -1;
+  for (int t = tid; t < kRows; t += kThr) sq[t] = t < len ? seg_of(p, f, bi, (long long)t0 + t) : -1;
   for (int k = tid; k < hpg; k += kThr) Ah[k] = f.A[h_first + k];
-  zero_padding(T, sXb, sYb, sB, sC, tid);  // B and C are contracted over tokens here
   if (tid < 32) tmem_alloc(tmem_slot, 512);
-  fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -233,8 +209,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       auto issue_dm = [&](int hh) {  // dM = dy x^T of head hh (M = i, N = j, K = headdim)
         const int buf = hh & 1;
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tDM + buf * 128, kdesc_tok(sYb + buf * kTok, ks), kdesc_tok(sXb + buf * kTok, ks), id128,
-                   ks > 0);
+          mma_bf16(tDM + buf * 128, kdesc_tok(sY(hh), ks), kdesc_tok(sX(hh), ks), id128, ks > 0);
         mma_commit(&b_dm[buf]);
       };
       if (!mbar_wait(&b_xy[0], 0)) ok = false;
@@ -243,8 +218,6 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       if (hpg == 1) mbar_arrive(b_fre);  // the parity-1 buffers are never used
       for (int hh = 0; hh < hpg; ++hh) {
         const int buf = hh & 1;
-        const uint8_t* sX = sXb + buf * kTok;
-        const uint8_t* sY = sYb + buf * kTok;
         const uint8_t* sS = sSb + buf * T.sbytes;
         const uint8_t* sH = sHb + buf * T.sbytes;
         // every warp is done with head hh-1: its dM buffer takes the next
@@ -252,7 +225,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
         if (hh >= 1 && hh + 1 < hpg && !mbar_wait(&b_dcb[buf ^ 1], ((hh - 1) >> 1) & 1)) ok = false;
         if (hh + 3 < hpg) issue_lq(hh + 3);
         if (hh + 1 < hpg) {
-          if (!mbar_wait(&b_xy[buf ^ 1], ((hh + 1) >> 1) & 1)) ok = false;
+          if (!mbar_wait(&b_xy[(hh + 1) % 3], ((hh + 1) / 3) & 1)) ok = false;
           tc_fence_after();
           issue_dm(hh + 1);
         }
@@ -261,22 +234,25 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
         if (!mbar_wait(&b_sh[buf], (hh >> 1) & 1)) ok = false;  // dS, H of head hh
         tc_fence_after();
         for (int ks = 0; ks < 4; ++ks) {
-          mma_bf16(tDC, kdesc_tok(sY, ks), kdesc_tok(sH, ks), idNk, (hh > 0 || ks > 0) ? 1u : 0u);
-          mma_bf16(tDB, kdesc_tok(sX, ks), kdesc_tok(sS, ks), idNk, (hh > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16(tDC, kdesc_tok(sY(hh), ks), kdesc_tok(sH, ks), idNk, (hh > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16(tDB, kdesc_tok(sX(hh), ks), kdesc_tok(sS, ks), idNk, (hh > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(b_cs);
-        // once the carry and state MMAs of head hh are done, its x/dy and
-        // dS/H buffers take the copies of head hh + 2
+        // once the carry and state MMAs of head hh are done, its x/dy slot
+        // takes head hh + 3 (or B, C at the end) and its dS/H buffers head hh + 2
         if (!mbar_wait(b_cs, hh & 1)) ok = false;
-        if (hh + 2 < hpg) {
-          issue_xy(hh + 2);
-          issue_sh(hh + 2);
+        if (hh + 3 < hpg) issue_xy(hh + 3);
+        if (hh + 2 < hpg) issue_sh(hh + 2);
+        if (hh + 3 == hpg) issue_bc(sB, &tmB, b_b);
+        if (hh + 2 == hpg) {
+          issue_bc(sC, &tmC, b_c);
+          mbar_arrive(b_fre);  // dS/H parity hpg & 1 holds no further head
         }
-        if (hh + 2 == hpg) mbar_arrive(b_fre);  // parity hpg & 1 holds no further head
       }
       // dC += S B (A K-major, K = j);  dB += S^T C (A MN-major, K = i)
       if (!mbar_wait(b_afin, 0)) ok = false;
-      if (!mbar_wait(b_bc, 0)) ok = false;
+      if (!mbar_wait(b_b, 0)) ok = false;
+      if (!mbar_wait(b_c, 0)) ok = false;
       tc_fence_after();
       const uint32_t a0 = smem_u32(sA0), lbo = smem_u32(sA1) - a0;
       for (int ks = 0; ks < kRows / 16; ++ks) {
@@ -306,12 +282,10 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
     const bool active = wg <= wq && j0 < len && wlane < len;  // warp-uniform
     for (int hh = 0; hh < hpg; ++hh) {
       const int buf = hh & 1;
-      uint8_t* sX = sXb + buf * kTok;
-      uint8_t* sY = sYb + buf * kTok;
-      const float* lb = lsl + (hh & 3) * 2 * p.Q;
-      const float* db = lb + p.Q;
+      const float* lb = lsl + (hh & 3) * 2 * kRows;
+      const float* db = lb + kRows;
       if (!mbar_wait(&b_lq[hh & 3], (hh >> 2) & 1)) ok = false;  // l, dt of head hh
-      if (!mbar_wait(&b_xy[buf], (hh >> 1) & 1)) ok = false;     // x, dy of head hh
+      if (!mbar_wait(&b_xy[hh % 3], (hh / 3) & 1)) ok = false;   // x, dy of head hh
       if (!mbar_wait(&b_dm[buf], (hh >> 1) & 1)) ok = false;     // dM of head hh has read them
       tc_fence_after();
       // row scaling in place, 32 rows x 32 columns per warp: warpgroups 0, 1
@@ -323,10 +297,10 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
         uint8_t* tile;
         if (wg < 2) {
           sc = (v && sq[t] == s_in) ? __expf(lb[t]) : 0.0f;
-          tile = sY;
+          tile = sY(hh);
         } else {
           sc = (v && sq[t] == s_last) ? __expf(lb[len - 1] - lb[t]) * db[t] : 0.0f;
-          tile = sX;
+          tile = sX(hh);
         }
         const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
@@ -467,7 +441,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
             tma_store_4d(&tmDC, sXb + (T.ncb + q) * kTok, q * 64, g, t0, bi);
           }
           bulk_commit();
-          bulk_wait_all();
+          bulk_wait_read<0>();  // shared memory is read; the writes complete on their own
         }
       }
     }
@@ -481,15 +455,15 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
 }  // namespace
 
 bool chunk_bwd_group_tc_supported(const Plan& p) {
-  return p.dtype == SSD_BF16 && p.P == 64 && (p.Q == 64 || p.Q == 128) &&
+  return p.dtype == SSD_BF16 && p.P == 64 && p.Q == kRows &&
          (p.N == 16 || p.N == 32 || p.N == 64 || p.N == 128) && p.hpg <= 256;
 }
 
 namespace {
 bool group_maps(const Plan& p, const Bufs& f, CUtensorMap* X, CUtensorMap* Y, CUtensorMap* B, CUtensorMap* C,
                 CUtensorMap* S, CUtensorMap* H, CUtensorMap* DB, CUtensorMap* DC) {
-  const GTiles T = gtiles(p.N, p.Q);
-  const uint32_t rows = (uint32_t)T.rows;
+  const GTiles T = gtiles(p.N);
+  const uint32_t rows = (uint32_t)kRows;
   const uint64_t dbc[4] = {(uint64_t)p.N, (uint64_t)p.G, (uint64_t)p.L, (uint64_t)p.b};
   const uint64_t sbc[3] = {(uint64_t)p.N * 2, (uint64_t)p.G * p.N * 2, (uint64_t)p.L * p.G * p.N * 2};
   const uint32_t bbc[4] = {(uint32_t)(T.cw / 2), 1, rows, 1};
@@ -508,10 +482,10 @@ bool group_maps(const Plan& p, const Bufs& f, CUtensorMap* X, CUtensorMap* Y, CU
 
 cudaError_t launch_chunk_bwd_dbc_group_tc(const Plan& p, const Bufs& f, cudaStream_t s) {
   set_kernel_name("chunk_bwd_dbc_tc");
-  const GTiles T = gtiles(p.N, p.Q);
+  const GTiles T = gtiles(p.N);
   CUtensorMap X, Y, B, C, S, H, DB, DC;
   if (!group_maps(p, f, &X, &Y, &B, &C, &S, &H, &DB, &DC)) return cudaErrorInvalidValue;
-  const size_t smem = group_smem_bytes(T, p.Q);
+  const size_t smem = group_smem_bytes(T);
   cudaError_t e = cudaFuncSetAttribute(chunk_bwd_dbc_group_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
