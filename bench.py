@@ -89,13 +89,14 @@ def kernel_model(cfg, dtype_bytes, keep=False):
     # (2 flops per multiply-add, dense tiles): the token kernel forms C B^T
     # once per group and, per head, dM = dy x^T, dX_s = B dS^T,
     # Y_c = C H_in^T and dX = M^T dY; the dB/dC kernel, per head, dM again,
-    # dC += dy H, dB += x dS, dC += dCB B and dB += dCB^T C.
+    # dC += dy H, dB += x dS; once per group on the heads' summed dCB, S B and S^T C.
     bwd_tok_flops = gunits * 2 * Q * Q * N + units * (4 * Q * Q * P + 4 * Q * P * N)
     bwd_dbc_flops = units * (2 * Q * Q * P + 4 * Q * N * P) + gunits * 4 * Q * Q * N
     # per-head token gradients (dx, ddt_eff, dl): x, dy, B, C, dS, H_in in; dx out
     m["chunk_bwd"] = dict(bytes=3 * tokx + 2 * tokbc + 2 * stS + 4 * per_tok, flops=bwd_tok_flops)
-    # group gradients dB, dC: x, dy, B, C, dS, H_in in; dB, dC out
-    m["chunk_bwd_dbc"] = dict(bytes=2 * tokx + 4 * tokbc + 2 * stS + 2 * per_tok,
+    # group gradients dB, dC: x, dy, B, C, dS, H_in, l, dt_eff in; dB, dC out;
+    # and the per-token ddt: dt, dL/dl, ddt_eff in, ddt out
+    m["chunk_bwd_dbc"] = dict(bytes=2 * tokx + 4 * tokbc + 2 * stS + 4 * per_tok + 2 * T * H * s,
                               flops=bwd_dbc_flops)
     m["dt_bwd"] = dict(bytes=2 * T * H * s + 4 * per_tok, flops=0)
     # the backward's state chains, one pass each: forward reads x, B, l, dt_eff

@@ -39,7 +39,7 @@ using namespace tc;
 
 constexpr int kRows = 128;
 constexpr int kCompute = 512;        // 16 compute warps: four read each quarter of the TMEM lanes
-constexpr int kThr = kCompute + 32;  // and one control warp for the copies and MMAs
+constexpr int kThr = kCompute + 96;  // one control warp for the copies and MMAs, two for ddt
 constexpr uint32_t kTok = kRows * 128u;  // one (128 tokens x 64) bf16 tile
 constexpr uint32_t kSlot = 2 * kTok;       // an x tile and a dy tile
 
@@ -76,13 +76,19 @@ __host__ __device__ inline GTiles gtiles(int N) {
 
 constexpr int kCw = kCompute / 32;  // compute warps: one arrival each on the per-head barriers
 constexpr int kMaxHpg = 256;
-constexpr int kBars = 22;
+constexpr int kBars = 26;
+constexpr int kRing = 4 * kRows;  // floats per scalar-ring slot: l, dt, dL/dl, ddt_eff
 
-// Scalars after the tiles: l and dt of four heads (a ring filled by bulk
-// copies), the segment ids, a 32-entry factor table per warp, A of the
-// group's heads; then the barriers and the tensor-memory address.
+// Scalars after the tiles: l, dt, dL/dl and ddt_eff of four heads (a ring
+// filled by bulk copies), the segment ids, a 32-entry factor table per warp,
+// A of the group's heads; then the barriers and the tensor-memory address.
 __host__ __device__ inline size_t group_smem_bytes(const GTiles& T) {
-  return 1024 + T.offF + (size_t)(9 * kRows + kCw * 32 + kMaxHpg) * 4 + kBars * 8 + 16;
+  return 1024 + T.offF + (size_t)(4 * kRing + kRows + kCw * 32 + kMaxHpg) * 4 + kBars * 8 + 16;
+}
+
+__device__ __forceinline__ float sigmoid_f(float z) {  // fast-math form; its result is rounded to bf16
+  const float e = __expf(-fabsf(z));
+  return z >= 0.0f ? __fdividef(1.0f, 1.0f + e) : __fdividef(e, 1.0f + e);
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -122,8 +128,8 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
   // buffers of parity hpg & 1 (no head after hpg - 2 is loaded there)
   uint8_t* sA0 = T.aliasA ? sSb + (hpg & 1) * T.sbytes : sm + T.offA;
   uint8_t* sA1 = T.aliasA ? sHb + (hpg & 1) * T.sbytes : sm + T.offA + kTok;
-  float* lsl = reinterpret_cast<float*>(sm + T.offF);  // [4 slots][l, dt][Q]
-  int* sq = reinterpret_cast<int*>(lsl + 8 * kRows);   // [Q]
+  float* lsl = reinterpret_cast<float*>(sm + T.offF);  // [4 slots][l, dt, dL/dl, ddt_eff][Q]
+  int* sq = reinterpret_cast<int*>(lsl + 4 * kRing);   // [Q]
   float* wtab = reinterpret_cast<float*>(sq + kRows);  // [warp][32] exp(l_r - l_j) dt_j
   float* Ah = wtab + kCw * 32;                         // [kMaxHpg]
   uint64_t* bar = reinterpret_cast<uint64_t*>(Ah + kMaxHpg);
@@ -132,15 +138,16 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
   // its part of the x, dy of head parity k; cs: carry/state MMAs done;
   // dcb[2]: every warp is done with the head of dM buffer k (its dM, its
   // scalars); fre: the S tile's buffers hold no further head; afin: S tile
-  // written; fin: final MMAs done; lq[4]: scalars of ring slot k loaded
+  // written; fin: final MMAs done; lq[4]: scalars of ring slot k loaded;
+  // dt[4]: the ddt warp is done with ring slot k
   uint64_t *b_b = bar, *b_c = bar + 1, *b_xy = bar + 2, *b_sh = bar + 5, *b_dm = bar + 7, *b_sc = bar + 9,
            *b_cs = bar + 11, *b_dcb = bar + 12, *b_fre = bar + 14, *b_afin = bar + 15, *b_fin = bar + 16,
-           *b_lq = bar + 17;
+           *b_lq = bar + 17, *b_dt = bar + 21;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kBars);
 
   const int c = blockIdx.x, g = blockIdx.y, bi = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool ctl = tid >= kCompute;
+  const bool ctl = warp == kCw;  // warps kCw + 1, kCw + 2 form ddt (even, odd heads)
   const int wg = (tid >> 7) & 3, r = tid & 127, wq = (tid >> 5) & 3;
   const int wlane = wq * 32;
   const int t0 = c * kRows, len = min(kRows, p.L - t0);
@@ -161,12 +168,16 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
     tma_load_4d(sSb + buf * T.sbytes, &tmS, &b_sh[buf], 0, 0, c, bi * p.H + h);
     tma_load_4d(sHb + buf * T.sbytes, &tmH, &b_sh[buf], 0, 0, c, bi * p.H + h);
   };
-  auto issue_lq = [&](int hh) {  // l and dt of head hh (Q floats each, 16-byte aligned) into slot hh % 4
+  // l, dt, dL/dl, ddt_eff of head hh (Q floats each, 16-byte aligned) into slot hh % 4
+  auto issue_lq = [&](int hh) {
     const int s = hh & 3;
     const long long o = (bh0 + hh) * p.Lp + t0;
-    mbar_expect_tx(&b_lq[s], 2 * kRows * 4);
-    bulk_load(lsl + s * 2 * kRows, f.lcs + o, kRows * 4, &b_lq[s]);
-    bulk_load(lsl + s * 2 * kRows + kRows, f.dte + o, kRows * 4, &b_lq[s]);
+    float* d = lsl + s * kRing;
+    mbar_expect_tx(&b_lq[s], 4 * kRows * 4);
+    bulk_load(d, f.lcs + o, kRows * 4, &b_lq[s]);
+    bulk_load(d + kRows, f.dte + o, kRows * 4, &b_lq[s]);
+    bulk_load(d + 2 * kRows, f.dl + o, kRows * 4, &b_lq[s]);
+    bulk_load(d + 3 * kRows, f.ddte + o, kRows * 4, &b_lq[s]);
   };
   auto issue_bc = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bb) {
     mbar_expect_tx(bb, c_bytes);
@@ -220,10 +231,8 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
         const int buf = hh & 1;
         const uint8_t* sS = sSb + buf * T.sbytes;
         const uint8_t* sH = sHb + buf * T.sbytes;
-        // every warp is done with head hh-1: its dM buffer takes the next
-        // head's dM, its scalar slot the scalars of head hh+3
+        // every warp is done with head hh-1: its dM buffer takes the next head's dM
         if (hh >= 1 && hh + 1 < hpg && !mbar_wait(&b_dcb[buf ^ 1], ((hh - 1) >> 1) & 1)) ok = false;
-        if (hh + 3 < hpg) issue_lq(hh + 3);
         if (hh + 1 < hpg) {
           if (!mbar_wait(&b_xy[(hh + 1) % 3], ((hh + 1) / 3) & 1)) ok = false;
           tc_fence_after();
@@ -238,6 +247,12 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
           mma_bf16(tDB, kdesc_tok(sX(hh), ks), kdesc_tok(sS, ks), idNk, (hh > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(b_cs);
+        // the scalar slot of head hh-1 takes head hh+3 once the ddt warp is
+        // done with it as well
+        if (hh + 3 < hpg) {
+          if (hh >= 1 && !mbar_wait(&b_dt[(hh - 1) & 3], ((hh - 1) >> 2) & 1)) ok = false;
+          issue_lq(hh + 3);
+        }
         // once the carry and state MMAs of head hh are done, its x/dy slot
         // takes head hh + 3 (or B, C at the end) and its dS/H buffers head hh + 2
         if (!mbar_wait(b_cs, hh & 1)) ok = false;
@@ -263,6 +278,98 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       }
       mma_commit(b_fin);
     }
+  } else if (warp > kCw) {
+    // ---------------- two ddt warps ----------------
+    // Per head, from the token-gradient kernel's dL/dl and ddt_eff of this
+    // chunk: dL/d(dA_k) = sum_{i >= k} dL/dl_i (a reverse cumsum in the
+    // chunk; the last token also takes the chunk-state weights' sum and
+    // a_c dL/da_c), ddt_eff_k += A_h dL/d(dA_k), ddt_k = ddt_eff_k
+    // sigmoid(dt_k + dt_bias_h), and the chunk's partials of dA_h and
+    // ddt_bias_h.  Warp kCw + 1 + k takes the heads of parity k; lane l owns
+    // tokens 4 l .. 4 l + 3; fixed shuffle orders.
+    const int h0w = warp - kCw - 1;
+    const __nv_bfloat16* dtr = static_cast<const __nv_bfloat16*>(f.dt);
+    __nv_bfloat16* ddt = static_cast<__nv_bfloat16*>(f.ddt);
+    constexpr int kR = kRows / 32;
+    // global inputs of one head, loaded one head ahead: dt of the lane's
+    // tokens, dt_bias, and the chunk's partial sums (lane k holds slot k)
+    struct In {
+      float dtv[kR];
+      float bias, u, a, dp;
+    };
+    auto load_in = [&](int hh, In& in) {
+      const int h = h_first + hh;
+      const long long bh = bh0 + hh;
+#pragma unroll
+      for (int k = 0; k < kR; ++k) {
+        const int i = lane * kR + k;
+        in.dtv[k] = i < len ? __bfloat162float(dtr[((long long)bi * p.L + t0 + i) * p.H + h]) : 0.0f;
+      }
+      in.bias = f.dt_bias[h];
+      in.u = lane < p.cb_ntb ? f.udu[(bh * p.nc + c) * p.cb_ntb + lane] : 0.0f;
+      in.a = f.achunk[bh * p.nc + c];
+      in.dp = lane < p.da_nsum ? f.dapart[(bh * p.nc + c) * p.da_stride + lane] : 0.0f;
+    };
+    In cur, nxt;
+    if (h0w < hpg) load_in(h0w, cur);
+    for (int hh = h0w; hh < hpg; hh += 2) {
+      const int h = h_first + hh;
+      if (hh + 2 < hpg) load_in(hh + 2, nxt);
+      // the last token's extra gradient: the chunk-state weights' sums, then
+      // a_c dL/da_c (fixed butterfly trees over the slots)
+      float extra = cur.u, da = cur.dp;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) {
+        extra += __shfl_xor_sync(0xffffffffu, extra, d);
+        da += __shfl_xor_sync(0xffffffffu, da, d);
+      }
+      if (cur.a != 0.0f) extra += cur.a * da;
+      const float bias = cur.bias, Ahh = Ah[hh];
+      const float* slot = lsl + (hh & 3) * kRing;
+      if (!mbar_wait(&b_lq[hh & 3], (hh >> 2) & 1)) ok = false;
+      float dl[kR];
+      float tot = 0.0f;
+#pragma unroll
+      for (int k = 0; k < kR; ++k) {
+        const int i = lane * kR + k;
+        const float v = i < len ? slot[2 * kRows + i] + (i == len - 1 ? extra : 0.0f) : 0.0f;
+        dl[k] = v;
+        tot += v;
+      }
+      float sfx = tot;  // suffix sums across lanes: lanes to the right hold later tokens
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const float o = __shfl_down_sync(0xffffffffu, sfx, d);
+        if (lane + d < 32) sfx += o;
+      }
+      float run = __shfl_down_sync(0xffffffffu, sfx, 1);  // sum over lanes > lane
+      if (lane == 31) run = 0.0f;
+      float pA = 0.0f, pb = 0.0f;
+#pragma unroll
+      for (int k = kR - 1; k >= 0; --k) {
+        const int i = lane * kR + k;
+        if (i < len) {
+          run += dl[k];
+          const float g = slot[3 * kRows + i] + Ahh * run;
+          const float v = g * sigmoid_f(cur.dtv[k] + bias);
+          ddt[((long long)bi * p.L + t0 + i) * p.H + h] = __float2bfloat16_rn(v);
+          pA += slot[kRows + i] * run;
+          pb += v;
+        }
+      }
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) {
+        pA += __shfl_xor_sync(0xffffffffu, pA, d);
+        pb += __shfl_xor_sync(0xffffffffu, pb, d);
+      }
+      if (lane == 0) {
+        f.pdA[((long long)bi * p.nc + c) * p.H + h] = pA;
+        f.pdb[((long long)bi * p.nc + c) * p.H + h] = pb;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b_dt[hh & 3]);
+      cur = nxt;
+    }
   } else {
     // ---------------- 16 compute warps, each on its own ----------------
     const int s_in = seg_in_of(p, f, bi, c);
@@ -282,7 +389,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
     const bool active = wg <= wq && j0 < len && wlane < len;  // warp-uniform
     for (int hh = 0; hh < hpg; ++hh) {
       const int buf = hh & 1;
-      const float* lb = lsl + (hh & 3) * 2 * kRows;
+      const float* lb = lsl + (hh & 3) * kRing;
       const float* db = lb + kRows;
       if (!mbar_wait(&b_lq[hh & 3], (hh >> 2) & 1)) ok = false;  // l, dt of head hh
       if (!mbar_wait(&b_xy[hh % 3], (hh / 3) & 1)) ok = false;   // x, dy of head hh

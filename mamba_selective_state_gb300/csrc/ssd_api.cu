@@ -320,7 +320,8 @@ int ssd_bwd(const ssd_problem* prob, const void* x, const void* dt, const float*
     SSD_LAUNCH(launch_state_passing(p, f, true, false, s));
   }
   SSD_LAUNCH(launch_chunk_bwd(p, f, s));
-  SSD_LAUNCH(launch_dt_bwd(p, f, s));
+  // the tensor-core dB/dC kernel also forms ddt and the dA, ddt_bias partials
+  if (!chunk_bwd_tc_supported(p)) SSD_LAUNCH(launch_dt_bwd(p, f, s));
   SSD_LAUNCH(launch_param_reduce(p, f, s));
   return SSD_OK;
 }
