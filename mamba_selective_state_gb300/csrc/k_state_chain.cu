@@ -26,8 +26,11 @@
 // order by the parameter-gradient kernel.
 //
 // Warps: 16 compute (warp w reads TMEM lane quarter w % 4), 1 control (TMA
-// and tcgen05.mma from one lane).  Three TMA stages, two w . T1 tiles, two
-// accumulators: the product of chunk k+1 runs while chunk k is folded.
+// and tcgen05.mma from one lane).  Three stages (T1, T2 and the chunk's l and
+// dt_eff), two w . T1 tiles, two accumulators: the product of chunk k+1 runs
+// while chunk k is folded.  The reverse chain's carry-in tiles (for dL/da_c)
+// come by tensor copies into two buffers, each issued about two steps before
+// its step reads it.
 #include "ssd_internal.cuh"
 #include "tc_common.cuh"
 #include "tma_host.h"
@@ -46,19 +49,25 @@ constexpr int kStages = 3;
 struct ChainGeom {
   int ncb;           // 64-column blocks of B/C along d_state
   uint32_t blk;      // bytes of one 128-row x 128-byte tile block
-  uint32_t stage;    // T1 block + ncb T2 blocks
-  uint32_t offXs, offBar, bytes;
+  uint32_t offScal;  // l and dt_eff of the stage's chunk (Q floats each), after its tiles
+  uint32_t stage;    // T1 block + ncb T2 blocks + the scalars
+  uint32_t hbytes;   // one carry-in tile (N rows of 64 bf16), reverse chain only
+  uint32_t offXs, offH, offBar, bytes;
 };
 
-__host__ __device__ inline ChainGeom chain_geom(int N) {
+__host__ __device__ inline ChainGeom chain_geom(int N, bool rev) {
   ChainGeom g;
   g.ncb = N / 64;
   g.blk = kQ * 128u;
-  g.stage = g.blk * (1u + g.ncb);
+  g.offScal = g.blk * (1u + g.ncb);
+  g.stage = g.offScal + 2u * kQ * 4u;  // a multiple of 1024
   // with d_state 64 the product reads a second (unused) 64-row column block
-  // past T2: the next stage's T1, or for the last stage the w . T1 tiles
+  // past T2: the scalars and the next stage's T1, or for the last stage the
+  // w . T1 tiles
+  g.hbytes = rev ? (uint32_t)N * 128u : 0u;
   g.offXs = kStages * g.stage;
-  g.offBar = g.offXs + 2u * g.blk;
+  g.offH = g.offXs + 2u * g.blk;
+  g.offBar = g.offH + 2u * g.hbytes;
   g.bytes = g.offBar + 256u;
   return g;
 }
@@ -85,10 +94,11 @@ __device__ __forceinline__ void wait_or_flag(uint64_t* bar, uint32_t parity, boo
 template <bool kRev>
 __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
                                                               const __grid_constant__ CUtensorMap tm1,
-                                                              const __grid_constant__ CUtensorMap tm2) {
+                                                              const __grid_constant__ CUtensorMap tm2,
+                                                              const __grid_constant__ CUtensorMap tmH) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const ChainGeom G = chain_geom(p.N);
+  const ChainGeom G = chain_geom(p.N, kRev);
   const int bi = blockIdx.x / p.H, h = blockIdx.x % p.H;
   const int g = h / p.hpg;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -96,8 +106,10 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
   const long long bh = (long long)bi * p.H + h;
   uint8_t* sXs = sm + G.offXs;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + G.offBar);
-  uint64_t *b_ld = bar, *b_xs = bar + 3, *b_full = bar + 5, *b_free = bar + 7, *b_done = bar + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 12);
+  uint8_t* sH = sm + G.offH;  // [2] carry-in tiles (reverse), 128-byte swizzled rows
+  uint64_t *b_ld = bar, *b_xs = bar + kStages, *b_full = b_xs + 2, *b_free = b_full + 2, *b_done = b_free + 2,
+           *b_h = b_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_h + 2);
   auto chunk_of = [&](int k) { return kRev ? nc - 1 - k : k; };
 
   if (tid == kCompute) {
@@ -108,6 +120,8 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
       mbar_init(&b_free[k], kCompute / 32);
     }
     mbar_init(b_done, 1);
+    mbar_init(&b_h[0], 1);
+    mbar_init(&b_h[1], 1);
     mbar_fence_init();
     prefetch_tmap(&tm1);
     prefetch_tmap(&tm2);
@@ -122,6 +136,7 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
   if (warp == kCompute / 32) {
     // ------------------------------ control ------------------------------
     if (lane == 0) {
+      // the stage of step k: T1, T2 and the chunk's l and dt_eff
       auto load = [&](int k) {
         const int s = k % kStages, c = chunk_of(k);
         uint8_t* st = sm + s * G.stage;
@@ -129,9 +144,17 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
         tma_load_4d(st, &tm1, &b_ld[s], 0, h, c * kQ, bi);
         for (int q = 0; q < G.ncb; ++q)
           tma_load_4d(st + (1 + q) * G.blk, &tm2, &b_ld[s], q * 64, g, c * kQ, bi);
+        bulk_load(st + G.offScal, f.lcs + bh * p.Lp + (long long)c * kQ, kQ * 4, &b_ld[s]);
+        bulk_load(st + G.offScal + kQ * 4, f.dte + bh * p.Lp + (long long)c * kQ, kQ * 4, &b_ld[s]);
+      };
+      // reverse: the carry-in tile of step k, for dL/da_c
+      auto load_hin = [&](int k) {
+        mbar_expect_tx(&b_h[k & 1], G.hbytes);
+        tma_load_4d(sH + (k & 1) * G.hbytes, &tmH, &b_h[k & 1], 0, 0, chunk_of(k), (int)bh);
       };
       const uint32_t idS = idesc_bf16(128, 64, 1, 1);
       for (int k = 0; k < kStages && k < nc; ++k) load(k);
+      if (kRev) load_hin(0);
       for (int k = 0; k < nc; ++k) {
         const int s = k % kStages, b = k & 1;
         wait_or_flag(&b_xs[b], (k >> 1) & 1, ok);
@@ -150,6 +173,12 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
         // from it before the compute warps signalled)
         wait_or_flag(b_done, k & 1, ok);
         if (k + kStages < nc) load(k + kStages);
+        // the carry-in tile of step k+1 goes where step k-1's was, once that
+        // step is done (about two steps before step k+1 reads it)
+        if (kRev && k + 1 < nc) {
+          if (k >= 1) wait_or_flag(&b_free[(k - 1) & 1], ((k - 1) >> 1) & 1, ok);
+          load_hin(k + 1);
+        }
       }
     }
   } else {
@@ -160,47 +189,45 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
     const bool nvalid = n < p.N;
     const bool hwarp = 32 * sq4 < p.N;  // warp-uniform
     const int* seqr = f.seq != nullptr ? f.seq + (long long)bi * p.L : nullptr;
-    const float* lrow = f.lcs + bh * p.Lp;
-    const float* drow = f.dte + bh * p.Lp;
     float v[16];
     {
       const float* src = kRev ? f.dfinal : f.init;
 #pragma unroll
       for (int k = 0; k < 16; ++k) v[k] = (src != nullptr && nvalid) ? src[(bh * p.P + p0 + k) * p.N + n] : 0.0f;
     }
-    // The per-token weight of this thread's row in step k, from scalars
-    // loaded two steps ahead (their latency hides behind two chunks of work).
+    // Per-step values loaded two steps ahead (their latency hides behind two
+    // chunks of work): the chunk's decay and, with seq_idx, the segment ids
+    // that decide this thread's row weight.  (The loads are unconditional,
+    // from clamped addresses, so that they can land in the registers that
+    // use them; the conditions apply at the use.)
     struct Raw {
-      float l, lref, d;
+      float a;  // the chunk's decay a_c
       int s, sref;
-      bool in;
     };
-    // (the loads are unconditional, from clamped addresses, so that they can
-    // land in the registers that use them; the conditions apply at the use)
     auto ld_raw = [&](int k) {
       Raw r;
       const int kk = k < nc ? k : nc - 1;
       const int c = chunk_of(kk), t0 = c * kQ, len = min(kQ, p.L - t0), row = tid >> 2;
       const int rr = row < len ? row : len - 1;
-      r.in = k < nc && row < len;
-      r.l = __ldg(lrow + t0 + rr);
-      r.d = __ldg(drow + t0 + rr);
-      r.lref = kRev ? 0.0f : __ldg(lrow + t0 + len - 1);
+      r.a = __ldg(f.achunk + bh * nc + c);
       r.s = seqr ? __ldg(seqr + t0 + rr) : 0;
       r.sref = seqr ? __ldg(seqr + (kRev ? (t0 > 0 ? t0 - 1 : 0) : t0 + len - 1)) : 0;
       return r;
     };
-    auto make_w = [&](const Raw& r) {
-      if (!r.in || r.s != r.sref) return 0.0f;
-      return kRev ? expf(r.l) : expf(r.lref - r.l) * r.d;
-    };
     // w . T1 of step k: thread -> row tid/4, two 16-byte pieces (the tile's
-    // swizzle permutes pieces within a row, so the scaled copy keeps it)
-    auto scale = [&](int k, float wv) {
+    // swizzle permutes pieces within a row, so the scaled copy keeps it); the
+    // row weight from the chunk's l and dt_eff that came with the stage
+    auto scale = [&](int k, const Raw& r) {
       const int s = k % kStages;
       const int row = tid >> 2, part = tid & 3;
       wait_or_flag(&b_ld[s], (k / kStages) & 1, ok);
-      const uint4* src = reinterpret_cast<const uint4*>(sm + s * G.stage + row * 128) + part * 2;
+      const uint8_t* st = sm + s * G.stage;
+      const float* sl = reinterpret_cast<const float*>(st + G.offScal);
+      const int c = chunk_of(k), len = min(kQ, p.L - c * kQ);
+      float wv = 0.0f;
+      if (row < len && r.s == r.sref)
+        wv = kRev ? expf(sl[row]) : expf(sl[len - 1] - sl[row]) * sl[kQ + row];
+      const uint4* src = reinterpret_cast<const uint4*>(st + row * 128) + part * 2;
       uint4* dst = reinterpret_cast<uint4*>(sXs + (k & 1) * G.blk + row * 128) + part * 2;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -215,28 +242,16 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
       __syncwarp();
       if (lane == 0) mbar_arrive(&b_xs[k & 1]);
     };
-    // reverse: this thread's 16 carry-in values of the next chunk, loaded one
-    // chunk ahead (they only enter dL/da_c)
-    auto load_h = [&](int k, uint4 (&hv)[2]) {
-      if (kRev && hwarp) {
-        const int kk = k < nc ? k : nc - 1, nn = nvalid ? n : 0;
-        const uint4* hp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(f.Hin) +
-                                                         ((bh * nc + chunk_of(kk)) * p.N + nn) * 64 + p0);
-        hv[0] = hp[0];
-        hv[1] = hp[1];
-      }
-    };
     // One step: chunk k's value is written out and the product of chunk k
     // folded in, while w . T1 of chunk k+1 is formed and the operands of the
     // steps ahead are in flight.  The prefetched registers ping-pong between
-    // two sets (r_use/h_use read here, r_fill/h_fill loaded here and read a
-    // step later), so no copy waits on a load still in flight.
-    auto step = [&](int k, Raw& r_fill, const Raw& r_use, uint4 (&h_fill)[2], const uint4 (&h_use)[2]) {
-      load_h(k + 1, h_fill);
+    // two sets (r_use read here, r_fill loaded here and read a step later),
+    // so no copy waits on a load still in flight.
+    auto step = [&](int k, Raw& r_fill, const Raw& r_use) {
+      const float a = r_fill.a;  // a_c of chunk k, loaded two steps ago (before the set is refilled)
       r_fill = ld_raw(k + 2);
-      if (k + 1 < nc) scale(k + 1, make_w(r_use));
+      if (k + 1 < nc) scale(k + 1, r_use);
       const int c = chunk_of(k), b = k & 1;
-      const float a = f.achunk[bh * nc + c];
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(kRev ? f.dS : f.Hin) + ((bh * nc + c) * p.N + n) * 64 + p0;
       float dpart = 0.0f;
       if (hwarp && nvalid) {
@@ -246,8 +261,12 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
         reinterpret_cast<uint4*>(out)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
         reinterpret_cast<uint4*>(out)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
         if (kRev) {  // dL/da_c partial: <G, H_in[c]> over this thread's 16 entries
-          const uint32_t hw[8] = {h_use[0].x, h_use[0].y, h_use[0].z, h_use[0].w,
-                                  h_use[1].x, h_use[1].y, h_use[1].z, h_use[1].w};
+          wait_or_flag(&b_h[b], (k >> 1) & 1, ok);
+          // row n of the tile, 16-byte pieces 2 wg and 2 wg + 1 (128-byte swizzle)
+          const uint8_t* hrow = sH + b * G.hbytes + n * 128;
+          const uint4 h0 = *reinterpret_cast<const uint4*>(hrow + (((2 * wg) ^ (n & 7)) << 4));
+          const uint4 h1 = *reinterpret_cast<const uint4*>(hrow + (((2 * wg + 1) ^ (n & 7)) << 4));
+          const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[e]));
@@ -274,12 +293,10 @@ __global__ void __launch_bounds__(kThr, 1) state_chain_kernel(Plan p, Bufs f,
     };
     // set j & 1 holds the operands of chunk j
     Raw r0 = ld_raw(0), r1 = ld_raw(1);
-    uint4 h0[2] = {}, h1[2] = {};
-    load_h(0, h0);
-    scale(0, make_w(r0));
+    scale(0, r0);
     for (int k = 0; k < nc; k += 2) {
-      step(k, r0, r1, h1, h0);
-      if (k + 1 < nc) step(k + 1, r1, r0, h0, h1);
+      step(k, r0, r1);
+      if (k + 1 < nc) step(k + 1, r1, r0);
     }
     if (kRev && f.dinit != nullptr && nvalid) {
 #pragma unroll
@@ -301,22 +318,31 @@ bool state_chain_supported(const Plan& p) {
 
 cudaError_t launch_state_chain(const Plan& p, const Bufs& f, bool reverse, cudaStream_t s) {
   set_kernel_name(reverse ? "state_chain_bwd" : "state_chain_fwd");
-  const ChainGeom G = chain_geom(p.N);
-  CUtensorMap tm1, tm2;
+  const ChainGeom G = chain_geom(p.N, reverse);
+  CUtensorMap tm1, tm2, tmH;
   const uint64_t d1[4] = {64, (uint64_t)p.H, (uint64_t)p.L, (uint64_t)p.b};
   const uint64_t s1[3] = {128, (uint64_t)p.H * 128, (uint64_t)p.L * p.H * 128};
   const uint32_t b1[4] = {64, 1, (uint32_t)kQ, 1};
   const uint64_t d2[4] = {(uint64_t)p.N, (uint64_t)p.G, (uint64_t)p.L, (uint64_t)p.b};
   const uint64_t s2[3] = {(uint64_t)p.N * 2, (uint64_t)p.G * p.N * 2, (uint64_t)p.L * p.G * p.N * 2};
   const uint32_t b2[4] = {64, 1, (uint32_t)kQ, 1};
+  // carry-in states (b, H, nc, N, P) bf16: one chunk's N x 64 tile per copy
+  const uint64_t dh[4] = {64, (uint64_t)p.N, (uint64_t)p.nc, (uint64_t)p.b * p.H};
+  const uint64_t sh[3] = {128, (uint64_t)p.N * 128, (uint64_t)p.nc * p.N * 128};
+  const uint32_t bh[4] = {64, (uint32_t)p.N, 1, 1};
   if (!encode_tmap_bf16_4d(&tm1, reverse ? f.dy : f.x, d1, s1, b1, 128) ||
       !encode_tmap_bf16_4d(&tm2, reverse ? f.C : f.B, d2, s2, b2, 128))
     return cudaErrorInvalidValue;
+  if (reverse) {
+    if (!encode_tmap_bf16_4d(&tmH, f.Hin, dh, sh, bh, 128)) return cudaErrorInvalidValue;
+  } else {
+    tmH = tm1;  // not read by the forward chain
+  }
   const size_t smem = 1024 + G.bytes;
   auto kern = reverse ? state_chain_kernel<true> : state_chain_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.b * p.H, kThr, smem, s>>>(p, f, tm1, tm2);
+  kern<<<p.b * p.H, kThr, smem, s>>>(p, f, tm1, tm2, tmH);
   return cudaGetLastError();
 }
 
