@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
           mma_bf16(tDM + buf * 128, kdesc_tok(sY(hh), ks), kdesc_tok(sX(hh), ks), id128, ks > 0);
         mma_commit(&b_dm[buf]);
       };
-      if (!mbar_wait(&b_xy[0], 0)) ok = false;
+      mbar_wait_flag(&b_xy[0], 0, ok);
       tc_fence_after();
       issue_dm(0);
       if (hpg == 1) mbar_arrive(b_fre);  // the parity-1 buffers are never used
@@ -232,15 +232,15 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
         const uint8_t* sS = sSb + buf * T.sbytes;
         const uint8_t* sH = sHb + buf * T.sbytes;
         // every warp is done with head hh-1: its dM buffer takes the next head's dM
-        if (hh >= 1 && hh + 1 < hpg && !mbar_wait(&b_dcb[buf ^ 1], ((hh - 1) >> 1) & 1)) ok = false;
+        if (hh >= 1 && hh + 1 < hpg) mbar_wait_flag(&b_dcb[buf ^ 1], ((hh - 1) >> 1) & 1, ok);
         if (hh + 1 < hpg) {
-          if (!mbar_wait(&b_xy[(hh + 1) % 3], ((hh + 1) / 3) & 1)) ok = false;
+          mbar_wait_flag(&b_xy[(hh + 1) % 3], ((hh + 1) / 3) & 1, ok);
           tc_fence_after();
           issue_dm(hh + 1);
         }
         // carry and state: dC += (scaled dy) H, dB += (scaled x) dS  (K = headdim)
-        if (!mbar_wait(&b_sc[buf], (hh >> 1) & 1)) ok = false;  // x, dy of head hh scaled in place
-        if (!mbar_wait(&b_sh[buf], (hh >> 1) & 1)) ok = false;  // dS, H of head hh
+        mbar_wait_flag(&b_sc[buf], (hh >> 1) & 1, ok);  // x, dy of head hh scaled in place
+        mbar_wait_flag(&b_sh[buf], (hh >> 1) & 1, ok);  // dS, H of head hh
         tc_fence_after();
         for (int ks = 0; ks < 4; ++ks) {
           mma_bf16(tDC, kdesc_tok(sY(hh), ks), kdesc_tok(sH, ks), idNk, (hh > 0 || ks > 0) ? 1u : 0u);
@@ -250,12 +250,12 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
         // the scalar slot of head hh-1 takes head hh+3 once the ddt warp is
         // done with it as well
         if (hh + 3 < hpg) {
-          if (hh >= 1 && !mbar_wait(&b_dt[(hh - 1) & 3], ((hh - 1) >> 2) & 1)) ok = false;
+          if (hh >= 1) mbar_wait_flag(&b_dt[(hh - 1) & 3], ((hh - 1) >> 2) & 1, ok);
           issue_lq(hh + 3);
         }
         // once the carry and state MMAs of head hh are done, its x/dy slot
         // takes head hh + 3 (or B, C at the end) and its dS/H buffers head hh + 2
-        if (!mbar_wait(b_cs, hh & 1)) ok = false;
+        mbar_wait_flag(b_cs, hh & 1, ok);
         if (hh + 3 < hpg) issue_xy(hh + 3);
         if (hh + 2 < hpg) issue_sh(hh + 2);
         if (hh + 3 == hpg) issue_bc(sB, &tmB, b_b);
@@ -265,9 +265,9 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
         }
       }
       // dC += S B (A K-major, K = j);  dB += S^T C (A MN-major, K = i)
-      if (!mbar_wait(b_afin, 0)) ok = false;
-      if (!mbar_wait(b_b, 0)) ok = false;
-      if (!mbar_wait(b_c, 0)) ok = false;
+      mbar_wait_flag(b_afin, 0, ok);
+      mbar_wait_flag(b_b, 0, ok);
+      mbar_wait_flag(b_c, 0, ok);
       tc_fence_after();
       const uint32_t a0 = smem_u32(sA0), lbo = smem_u32(sA1) - a0;
       for (int ks = 0; ks < kRows / 16; ++ks) {
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       if (cur.a != 0.0f) extra += cur.a * da;
       const float bias = cur.bias, Ahh = Ah[hh];
       const float* slot = lsl + (hh & 3) * kRing;
-      if (!mbar_wait(&b_lq[hh & 3], (hh >> 2) & 1)) ok = false;
+      mbar_wait_flag(&b_lq[hh & 3], (hh >> 2) & 1, ok);
       float dl[kR];
       float tot = 0.0f;
 #pragma unroll
@@ -391,9 +391,9 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       const int buf = hh & 1;
       const float* lb = lsl + (hh & 3) * kRing;
       const float* db = lb + kRows;
-      if (!mbar_wait(&b_lq[hh & 3], (hh >> 2) & 1)) ok = false;  // l, dt of head hh
-      if (!mbar_wait(&b_xy[hh % 3], (hh / 3) & 1)) ok = false;   // x, dy of head hh
-      if (!mbar_wait(&b_dm[buf], (hh >> 1) & 1)) ok = false;     // dM of head hh has read them
+      mbar_wait_flag(&b_lq[hh & 3], (hh >> 2) & 1, ok);  // l, dt of head hh
+      mbar_wait_flag(&b_xy[hh % 3], (hh / 3) & 1, ok);   // x, dy of head hh
+      mbar_wait_flag(&b_dm[buf], (hh >> 1) & 1, ok);     // dM of head hh has read them
       tc_fence_after();
       // row scaling in place, 32 rows x 32 columns per warp: warpgroups 0, 1
       // -> cv e^{l} dy (rows i), 2, 3 -> u x (rows j)
@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       if (lane == 0) mbar_arrive(&b_dcb[buf]);
     }
     // S as a bf16 tile (rows i, K-major over j), once its buffers are free
-    if (!mbar_wait(b_fre, 0)) ok = false;
+    mbar_wait_flag(b_fre, 0, ok);
     {
       uint8_t* blk = (wg >> 1) ? sA1 : sA0;
 #pragma unroll
@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
     fence_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(b_afin);
-    if (!mbar_wait(b_fin, 0)) ok = false;  // the final dB/dC MMAs
+    mbar_wait_flag(b_fin, 0, ok);  // the final dB/dC MMAs
     tc_fence_after();
     // epilogue: rows of dB and dC (thread = token t; d_state columns 16 q, q = wg mod 4).
     // With 128-byte rows (d_state >= 64) they are staged in the x and dy

@@ -215,9 +215,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
   // C B^T | [2] (Z | W) | dXs | Yc
   const uint32_t tCB = tm, tZW = tm + 128, tDXS = tm + 384, tYC = tm + 448;
   bool ok = true;
-  auto wait = [&](uint64_t* b, uint32_t ph) {
-    if (!mbar_wait(b, ph)) ok = false;
-  };
+  auto wait = [&](uint64_t* b, uint32_t ph) { mbar_wait_flag(b, ph, ok); };
 
   if (warp >= kCompute / 32) {
     const int cw = warp - kCompute / 32;

@@ -71,6 +71,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// Bounded wait that records an expiry in `ok`; once a wait of this thread has
+// expired, later ones poll only briefly, so a kernel whose barriers no longer
+// complete still finishes in bounded time.
+__device__ __forceinline__ void mbar_wait_flag(uint64_t* bar, uint32_t parity, bool& ok) {
+  if (ok) {
+    if (!mbar_wait(bar, parity)) ok = false;
+    return;
+  }
+  for (int i = 0; i < 4096; ++i)
+    if (mbar_try_wait(bar, parity)) return;
+}
+
 // Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
 // from global to shared memory, completing on `bar` (transaction bytes).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
