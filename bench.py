@@ -133,10 +133,10 @@ def kernel_model(cfg, dtype_bytes, keep=False):
 # is the one captured, else null.
 NCU_TRAFFIC_WORKLOAD = "b2_L8192_bf16"
 NCU_TRAFFIC = {
-    "ssd_fwd_fused": (('k_ssd_fwd_fused.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.2900e+08, "e569469103a3af28fe8572ea6b03f51100cfd52b"),
-    "state_chain_bwd": (('k_state_chain.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.0840e+08, "bd67983a19538bba05afee85e87c61b7c763348a"),
-    "chunk_bwd_tc": (('k_chunk_bwd_tok_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.3850e+08, "7e4ae68fcb79f1d97acfa831397e3dcc121a9bb5"),
-    "chunk_bwd_dbc_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.6595e+08, "5574740bf6ecfc4db978c375aaa42b790b8a9b88"),
+    "ssd_fwd_fused": (('k_ssd_fwd_fused.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.2920e+08, "4ddc8fb9d33d304d9556a00f82c613cbd1f0ac0f"),
+    "state_chain_bwd": (('k_state_chain.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.1255e+08, "48084b3c61770d52a92ca2cf77406050e6c31a2f"),
+    "chunk_bwd_tc": (('k_chunk_bwd_tok_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.4065e+08, "fec74e23001b742b54dda9ef3a6f587703d9cd90"),
+    "chunk_bwd_dbc_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.9390e+08, "7d2863d97e108025ee3d156c291a6e5873832f9a"),
 }
 
 
