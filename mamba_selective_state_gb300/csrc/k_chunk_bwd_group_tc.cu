@@ -52,8 +52,7 @@ struct GTiles {
   uint32_t offX, offS, offH, offA, offF;
 };
 
-// Shared memory: three (x, dy) slots, each x then dy (slots 0 and 1 also
-// stage the dB/dC rows at the end), dS[2], H[2], the bf16 S tile (at
+// Shared memory: three (x, dy) slots, each x then dy, dS[2], H[2], the bf16 S tile (at
 // d_state 128 in the dS/H buffers that the last two heads leave free), then
 // the scalars.  B and C are only needed by the two final products: they
 // arrive in the x/dy slots that the last heads leave free.
@@ -99,19 +98,13 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
 }
 
-__device__ __forceinline__ void named_sync_compute() {  // the 16 compute warps only
-  asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
-}
-
 __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p, Bufs f,
                                                                         const __grid_constant__ CUtensorMap tmX,
                                                                         const __grid_constant__ CUtensorMap tmY,
                                                                         const __grid_constant__ CUtensorMap tmB,
                                                                         const __grid_constant__ CUtensorMap tmC,
                                                                         const __grid_constant__ CUtensorMap tmS,
-                                                                        const __grid_constant__ CUtensorMap tmH,
-                                                                        const __grid_constant__ CUtensorMap tmDB,
-                                                                        const __grid_constant__ CUtensorMap tmDC) {
+                                                                        const __grid_constant__ CUtensorMap tmH) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const GTiles T = gtiles(p.N);
@@ -502,15 +495,11 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
     if (lane == 0) mbar_arrive(b_afin);
     mbar_wait_flag(b_fin, 0, ok);  // the final dB/dC MMAs
     tc_fence_after();
-    // epilogue: rows of dB and dC (thread = token t; d_state columns 16 q, q = wg mod 4).
-    // With 128-byte rows (d_state >= 64) they are staged in the x and dy
-    // tiles, free once the final products are done, in the layout of a
-    // tensor copy, and leave by tensor stores (rows past the sequence are
-    // clipped); narrower states take plain stores.
+    // epilogue: rows of dB and dC (thread = token t; d_state columns 16 q,
+    // q = wg mod 4), 32-byte stores straight from registers (rows past the
+    // sequence are skipped)
     {
       const int t = r;
-      const bool v = t < len;
-      const bool staged = T.cw == 128;
       __nv_bfloat16* dB = static_cast<__nv_bfloat16*>(f.dB);
       __nv_bfloat16* dC = static_cast<__nv_bfloat16*>(f.dC);
       const long long row = (((long long)bi * p.L + t0 + t) * p.G + g) * p.N;
@@ -518,37 +507,13 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_dbc_group_tc_kernel(Plan p,
       for (int q = wg; q < nq; q += 4) {
         float vb[16], vc[16];
         tmem_ld16x2(tmem_addr(tDB, wlane, q * 16), tmem_addr(tDC, wlane, q * 16), vb, vc);
-        const uint4 b0 = make_uint4(pack2(vb[0], vb[1]), pack2(vb[2], vb[3]), pack2(vb[4], vb[5]), pack2(vb[6], vb[7]));
-        const uint4 b1 = make_uint4(pack2(vb[8], vb[9]), pack2(vb[10], vb[11]), pack2(vb[12], vb[13]), pack2(vb[14], vb[15]));
-        const uint4 c0 = make_uint4(pack2(vc[0], vc[1]), pack2(vc[2], vc[3]), pack2(vc[4], vc[5]), pack2(vc[6], vc[7]));
-        const uint4 c1 = make_uint4(pack2(vc[8], vc[9]), pack2(vc[10], vc[11]), pack2(vc[12], vc[13]), pack2(vc[14], vc[15]));
-        if (staged) {
-          uint8_t* sb = sXb + (q >> 2) * kTok;            // dB column block q / 4
-          uint8_t* sc = sXb + (T.ncb + (q >> 2)) * kTok;  // dC column block q / 4
-          const uint32_t e0 = (q & 3) * 16;
-          *reinterpret_cast<uint4*>(sb + swz128_off(t, e0)) = b0;
-          *reinterpret_cast<uint4*>(sb + swz128_off(t, e0 + 8)) = b1;
-          *reinterpret_cast<uint4*>(sc + swz128_off(t, e0)) = c0;
-          *reinterpret_cast<uint4*>(sc + swz128_off(t, e0 + 8)) = c1;
-        } else if (v) {
+        if (t < len) {
           uint4* ob = reinterpret_cast<uint4*>(dB + row + q * 16);
           uint4* oc = reinterpret_cast<uint4*>(dC + row + q * 16);
-          ob[0] = b0;
-          ob[1] = b1;
-          oc[0] = c0;
-          oc[1] = c1;
-        }
-      }
-      if (staged) {
-        fence_async_smem();
-        named_sync_compute();
-        if (tid == 0) {
-          for (int q = 0; q < T.ncb; ++q) {
-            tma_store_4d(&tmDB, sXb + q * kTok, q * 64, g, t0, bi);
-            tma_store_4d(&tmDC, sXb + (T.ncb + q) * kTok, q * 64, g, t0, bi);
-          }
-          bulk_commit();
-          bulk_wait_read<0>();  // shared memory is read; the writes complete on their own
+          ob[0] = make_uint4(pack2(vb[0], vb[1]), pack2(vb[2], vb[3]), pack2(vb[4], vb[5]), pack2(vb[6], vb[7]));
+          ob[1] = make_uint4(pack2(vb[8], vb[9]), pack2(vb[10], vb[11]), pack2(vb[12], vb[13]), pack2(vb[14], vb[15]));
+          oc[0] = make_uint4(pack2(vc[0], vc[1]), pack2(vc[2], vc[3]), pack2(vc[4], vc[5]), pack2(vc[6], vc[7]));
+          oc[1] = make_uint4(pack2(vc[8], vc[9]), pack2(vc[10], vc[11]), pack2(vc[12], vc[13]), pack2(vc[14], vc[15]));
         }
       }
     }
@@ -568,7 +533,7 @@ bool chunk_bwd_group_tc_supported(const Plan& p) {
 
 namespace {
 bool group_maps(const Plan& p, const Bufs& f, CUtensorMap* X, CUtensorMap* Y, CUtensorMap* B, CUtensorMap* C,
-                CUtensorMap* S, CUtensorMap* H, CUtensorMap* DB, CUtensorMap* DC) {
+                CUtensorMap* S, CUtensorMap* H) {
   const GTiles T = gtiles(p.N);
   const uint32_t rows = (uint32_t)kRows;
   const uint64_t dbc[4] = {(uint64_t)p.N, (uint64_t)p.G, (uint64_t)p.L, (uint64_t)p.b};
@@ -582,21 +547,20 @@ bool group_maps(const Plan& p, const Bufs& f, CUtensorMap* X, CUtensorMap* Y, CU
   const uint32_t bs[4] = {64, (uint32_t)p.N, 1, 1};
   return encode_tmap_bf16_4d(X, f.x, dxx, sxx, bxx, 128) && encode_tmap_bf16_4d(Y, f.dy, dxx, sxx, bxx, 128) &&
          encode_tmap_bf16_4d(B, f.B, dbc, sbc, bbc, T.cw) && encode_tmap_bf16_4d(C, f.C, dbc, sbc, bbc, T.cw) &&
-         encode_tmap_bf16_4d(S, f.dS, ds, ss, bs, 128) && encode_tmap_bf16_4d(H, f.Hin, ds, ss, bs, 128) &&
-         encode_tmap_bf16_4d(DB, f.dB, dbc, sbc, bbc, T.cw) && encode_tmap_bf16_4d(DC, f.dC, dbc, sbc, bbc, T.cw);
+         encode_tmap_bf16_4d(S, f.dS, ds, ss, bs, 128) && encode_tmap_bf16_4d(H, f.Hin, ds, ss, bs, 128);
 }
 }  // namespace
 
 cudaError_t launch_chunk_bwd_dbc_group_tc(const Plan& p, const Bufs& f, cudaStream_t s) {
   set_kernel_name("chunk_bwd_dbc_tc");
   const GTiles T = gtiles(p.N);
-  CUtensorMap X, Y, B, C, S, H, DB, DC;
-  if (!group_maps(p, f, &X, &Y, &B, &C, &S, &H, &DB, &DC)) return cudaErrorInvalidValue;
+  CUtensorMap X, Y, B, C, S, H;
+  if (!group_maps(p, f, &X, &Y, &B, &C, &S, &H)) return cudaErrorInvalidValue;
   const size_t smem = group_smem_bytes(T);
   cudaError_t e = cudaFuncSetAttribute(chunk_bwd_dbc_group_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  chunk_bwd_dbc_group_tc_kernel<<<dim3(p.nc, p.G, p.b), kThr, smem, s>>>(p, f, X, Y, B, C, S, H, DB, DC);
+  chunk_bwd_dbc_group_tc_kernel<<<dim3(p.nc, p.G, p.b), kThr, smem, s>>>(p, f, X, Y, B, C, S, H);
   return cudaGetLastError();
 }
 
