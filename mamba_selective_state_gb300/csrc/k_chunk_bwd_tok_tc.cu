@@ -87,11 +87,11 @@ __host__ __device__ inline TokGeom tok_geom(int N) {
 }
 
 // floats after offF: l, dt [3 slots][Q]; segment ids [4 units][Q]; unit
-// table [4][8]; factor table [3][Q];
+// table [4][8]; a 32-entry factor table per compute warp [16][32];
 // five partial arrays [4][Q]; per-warp sums [8]; then the barriers and the
 // TMEM address
 constexpr int kRingU = 4;  // units whose segment ids and coordinates are kept
-constexpr int kFloats = 3 * kQ + 3 * kQ + kRingU * kQ + kRingU * 8 + 3 * kQ + 20 * kQ + 8;
+constexpr int kFloats = 3 * kQ + 3 * kQ + kRingU * kQ + kRingU * 8 + 4 * kQ + 20 * kQ + 8;
 
 __host__ __device__ inline size_t tok_smem_bytes(const TokGeom& T) {
   return 1024 + T.offF + (size_t)kFloats * 4 + 16 * 8 + 16;
@@ -154,8 +154,8 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
   float* dtq = lq + 3 * kQ;                           // [3][Q]
   int* sqr = reinterpret_cast<int*>(dtq + 3 * kQ);    // [kRingU][Q] segment ids
   int* utab = sqr + kRingU * kQ;                      // [kRingU][8] unit table
-  float* sfac = reinterpret_cast<float*>(utab + kRingU * 8);  // [3][Q] exp(l_{32 rb} - l_j) dt_j, rb = 1..3
-  float* pZX = sfac + 3 * kQ;                         // [4 warpgroups][Q] x . Z
+  float* wtab = reinterpret_cast<float*>(utab + kRingU * 8);  // [warp][32] exp(l_r - l_j) dt_j
+  float* pZX = wtab + 4 * kQ;                         // [4 warpgroups][Q] x . Z
   float* pWY = pZX + 4 * kQ;                          // dy . W
   float* pDU = pWY + 4 * kQ;                          // x . dXs
   float* pCA = pDU + 4 * kQ;                          // dy . Yc
@@ -195,7 +195,8 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
     }
   };
   if (tid == kCompute) {
-    for (int k = 0; k < 11; ++k) mbar_init(&bar[k], 1);  // bc, xy[2], sh, cb, b1, mr, b2[2], ed[2]
+    // bc, xy[2], sh, cb, b1, mr (one arrival per compute warp), b2[2], ed[2]
+    for (int k = 0; k < 11; ++k) mbar_init(&bar[k], bar + k == b_mr ? kCompute / 32 : 1);
     mbar_init(b_bf, kCompute / 32);                      // one arrival per compute warp
     mbar_fence_init();
   }
@@ -354,17 +355,6 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
   } else if (nh > 0) {
     // ---------------- 16 compute warps ----------------
     const int i_row = wlane + lane;  // row of this thread in the mask pass
-    // per-head factor table exp(l_{32 rb} - l_j) dt_j (j < 32 rb) of head k of unit iu
-    auto fill_fac = [&](int k, int iu) {
-      if (tid < 3 * kQ) {
-        const int slot = k % 3, rb = 1 + tid / kQ, j = tid % kQ;
-        const int len = utab[(iu % kRingU) * 8 + kUlen];
-        const float* lb = lq + slot * kQ;
-        const float* db = dtq + slot * kQ;
-        sfac[tid] = (j < 32 * rb && j < len) ? __expf(lb[32 * rb] - lb[j]) * db[j] : 0.0f;
-      }
-    };
-    fill_fac(0, 0);
     // upper-triangle 16-column units of the M tile: zero once
     for (int q = 2 * wq + 2 + wg; q < 8; q += 4) {
       uint8_t* blk = sA + (q >> 2) * kTok;
@@ -411,6 +401,14 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
       const bool fact = one_seg && f.A[ut[kUg] * hpg + hh] <= 0.0f;
       const float li = tok_ok ? lb[i_row] : lb[len - 1];
       const float r_row = wq > 0 ? __expf(li - lb[32 * wq]) : 0.0f;
+      // this warp's factor table: exp(l_r - l_j) dt_j (l_r the l of the row
+      // block's first row) for the columns of its units q = wg and wg + 4
+      float* tab = wtab + warp * 32;
+      if (fact && wg < 2 * wq) {  // warp-uniform: the warp has a factored unit
+        const int j = lane < 16 ? 16 * wg + lane : 16 * (wg + 4) + lane - 16;
+        tab[lane] = (j < 32 * wq && j < len) ? __expf(lb[32 * wq] - lb[j]) * db[j] : 0.0f;
+        __syncwarp();
+      }
       for (int q = wg; q <= 2 * wq + 1; q += 4) {
         const int j0 = q * 16;
         uint32_t pk[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -418,10 +416,10 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
           float v[16];
           tmem_ld16(tmem_addr(tCB, wlane, j0), v);
           if (fact && q < 2 * wq) {
-            const float* s = sfac + (wq - 1) * kQ;
+            const float* s = tab + (q == wg ? 0 : 16);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const float4 sj = *reinterpret_cast<const float4*>(s + j0 + 4 * kk);
+              const float4 sj = *reinterpret_cast<const float4*>(s + 4 * kk);
               pk[2 * kk] = pack2(v[4 * kk] * sj.x * r_row, v[4 * kk + 1] * sj.y * r_row);
               pk[2 * kk + 1] = pack2(v[4 * kk + 2] * sj.z * r_row, v[4 * kk + 3] * sj.w * r_row);
             }
@@ -450,15 +448,13 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
         *reinterpret_cast<uint4*>(blk + swz128_off(i_row, e0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         *reinterpret_cast<uint4*>(blk + swz128_off(i_row, e0 + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
-      cp_async_wait_all();  // scalars of head k+1 landed (visible after the barrier)
+      // this thread's scalar copies of head k+1 landed (visible to the other
+      // warps after the next CTA-wide barrier, which precedes that head's passes)
+      cp_async_wait_all();
       fence_async_smem();
       tc_fence_before();
-      named_sync_compute();  // M complete; C B^T reads of this head done
-      if (tid == 0) mbar_arrive(b_mr);
-      // factor table of the next head: its scalars are visible since the
-      // barrier, and this head's mask pass is done with the table; a later
-      // barrier orders it before that head's mask pass
-      if (k + 1 < nh) fill_fac(k + 1, iu_n);
+      __syncwarp();  // the warp's part of M is written, its C B^T reads done
+      if (lane == 0) mbar_arrive(b_mr);
     };
 
     // ---- epilogue of head e (head eh of unit eu): token t = r, headdim columns 16 wg ..
@@ -582,7 +578,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
       if (k < nh) {
         mask_pass(k, iu, hh);
         if (k >= 1 && !epi_first) epilogue(k - 1, eu, eh);
-        else named_sync_compute();  // the factor table before the next mask pass
+        else named_sync_compute();  // the next head's scalars before its passes
       }
       eu = iu;
       eh = hh;
