@@ -117,7 +117,11 @@ enum {
    * SSD_PATH_MULTI_KERNEL forces the separate kernels; SSD_PATH_SINGLE_PASS
    * forces the single-pass kernels wherever their shape set allows. */
   SSD_PATH_MULTI_KERNEL = 1 << 17,
-  SSD_PATH_SINGLE_PASS = 1 << 18
+  SSD_PATH_SINGLE_PASS = 1 << 18,
+  /* Testing only: the persistent token-gradient kernel runs on at most two
+   * CTAs, so that a small problem walks several work units per CTA.  Results
+   * are the same bits as without the flag. */
+  SSD_TEST_FEW_CTAS = 1 << 19
 };
 
 typedef struct {

@@ -626,7 +626,7 @@ cudaError_t launch_chunk_bwd_tok_tc(const Plan& p, const Bufs& f, cudaStream_t s
   // columns), at most one per work unit
   const long long units = (long long)p.nc * p.G * p.b;
   if (units >= (1ll << 31)) return cudaErrorInvalidValue;
-  const long long sms = device_sm_count();
+  const long long sms = (p.flags & SSD_TEST_FEW_CTAS) ? 2 : device_sm_count();
   const int grid = (int)(units < sms ? units : sms);
   chunk_bwd_tok_tc_kernel<<<grid, kThr, smem, s>>>(p, f, X, Y, B, C, S, H, DX);
   return cudaGetLastError();

@@ -92,6 +92,27 @@ def test_small_parity(name):
     assert_close(got, ref, inp.dtype)
 
 
+# tensor-core backward: one to eight heads per group, sequence starts on
+# chunk boundaries and inside chunks, d_state 16 to 128
+FEW_CTAS = ["bf16_N16_Q64", "bf16_Q256_init", "bf16_chunk_aligned_resets", "bf16_N64_G4_varlen"]
+
+
+@pytest.mark.parametrize("name", FEW_CTAS)
+def test_persistent_kernels_walk_several_units(name):
+    """The persistent token-gradient kernel on two CTAs (SSD_TEST_FEW_CTAS),
+    so that each CTA of a small problem walks several work units in turn (the
+    copies and products of one unit's first head overlapping the previous
+    unit's last heads): the same bits as with one CTA per unit, and the
+    oracle's values."""
+    from mamba_selective_state_gb300 import _lib
+    inp = make_inputs(seed=5, **SMALL[name])
+    _, one = run_device(inp)
+    _, few = run_device(inp, extra_flags=_lib.SSD_TEST_FEW_CTAS)
+    for k in one:
+        assert torch.equal(one[k], few[k]), k
+    assert_close(few, oracle_full(inp), inp.dtype)
+
+
 # bf16, headdim 64, d_state 64 or 128: the single-pass forward's shape set
 SINGLE_PASS = ["bf16_N128_G2", "bf16_N64_G4_varlen", "bf16_Q256_init", "bf16_single_token",
                "bf16_shorter_than_chunk", "bf16_Q32_mixed", "bf16_chunk_aligned_resets", "bf16_two_chunks",
