@@ -389,7 +389,10 @@ def step_flags(args):
     backward would recompute, and the backward takes them (the usual
     training step); --recompute benchmarks the stateless backward."""
     from mamba_selective_state_gb300 import _lib
-    return 0 if args.recompute else _lib.SSD_KEEP_FWD_STATES
+    flags = 0 if args.recompute else _lib.SSD_KEEP_FWD_STATES
+    if getattr(args, "scan", "sequential") == "warp_shuffle":
+        flags |= _lib.SSD_SCAN_WARP_SHUFFLE
+    return flags
 
 
 # ----------------------------------------------------------------------------
@@ -543,7 +546,9 @@ def run_gpu(args, world, rank, local):
                                    "inputs larger than L2", parallelism="replicas" if world > 1
                            else "single GPU",
                            fwd_intermediates="recomputed by the backward" if args.recompute else
-                           "kept by the forward for the backward (SSD_KEEP_FWD_STATES)"),
+                           "kept by the forward for the backward (SSD_KEEP_FWD_STATES)",
+                           **({"scan": "warp_shuffle (SSD_SCAN_WARP_SHUFFLE)"}
+                              if args.scan == "warp_shuffle" else {})),
             "roofline": roof, "layer_roofline": layer, "e2e": e2e,
             "gpu_launches": launches, "kernels": kernels, "clocks": clk,
             "wall_s_timed": t_wall,
@@ -929,6 +934,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scan", default="sequential", choices=["sequential", "warp_shuffle"],
+                    help="the separate kernels' forward state-passing scan: each thread scans its "
+                         "elements over a segment's chunks (default), or the lanes of a warp hold "
+                         "the chunks and warp shuffles compose them (comparison)")
     ap.add_argument("--recompute", action="store_true",
                     help="the backward recomputes the forward's intermediates instead of taking "
                          "the ones the step's forward kept")

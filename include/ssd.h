@@ -121,7 +121,13 @@ enum {
   /* Testing only: the persistent token-gradient kernel runs on at most two
    * CTAs, so that a small problem walks several work units per CTA.  Results
    * are the same bits as without the flag. */
-  SSD_TEST_FEW_CTAS = 1 << 19
+  SSD_TEST_FEW_CTAS = 1 << 19,
+  /* Comparison: the separate kernels' forward state-passing scan takes each
+   * segment's local scan across the lanes of a warp (Hillis-Steele steps of
+   * warp shuffles, lane k holding chunk k) instead of sequentially inside
+   * each thread; the join of the segments is the same.  Results agree to
+   * rounding. */
+  SSD_SCAN_WARP_SHUFFLE = 1 << 20
 };
 
 typedef struct {

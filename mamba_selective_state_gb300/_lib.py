@@ -31,6 +31,7 @@ SSD_TEST_DROP_SCAN_PUBLISH = 1 << 16
 SSD_PATH_MULTI_KERNEL = 1 << 17
 SSD_PATH_SINGLE_PASS = 1 << 18
 SSD_TEST_FEW_CTAS = 1 << 19
+SSD_SCAN_WARP_SHUFFLE = 1 << 20
 SSD_NORM_HAS_Z = 1
 
 # every symbol include/ssd.h declares

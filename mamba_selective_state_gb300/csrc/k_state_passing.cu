@@ -102,8 +102,15 @@ __host__ __device__ constexpr int sp_seg() { return kBwd ? kSpSegB : kSpSegF; }
 template <bool kBwd>
 __host__ __device__ constexpr size_t sp_smem_bytes() { return (size_t)sp_seg<kBwd>() * kSpElems * 4 * (kBwd ? 2 : 1); }
 
-template <bool kBwd, bool kKeepF32, typename TOut>
+// kShfl (forward only; SSD_SCAN_WARP_SHUFFLE): the segment's local scans
+// run across lanes instead of inside a thread -- lane k of a group of kSeg
+// lanes holds chunk k of one float4 of elements, and log2(kSeg) Hillis-Steele
+// steps of warp shuffles compose the pairs (a, b) o (a', b') = (a a', a' b + b')
+// -- with the per-thread aggregates and prefixes staged through shared memory
+// for the join.  Kept for comparison with the in-thread sequential scan.
+template <bool kBwd, bool kKeepF32, typename TOut, bool kShfl = false>
 __global__ void __launch_bounds__(kSpThreads, 3) state_passing_kernel(Plan p, Bufs f) {
+  static_assert(!(kShfl && kBwd), "the warp-shuffle variant is forward only");
   constexpr int kSeg = sp_seg<kBwd>();
   extern __shared__ __align__(128) float s_buf[];  // [kSeg][kSpElems] inputs; reverse: then [kSeg][kSpElems] H_in
   __shared__ __align__(8) uint64_t s_bar;
@@ -158,8 +165,40 @@ __global__ void __launch_bounds__(kSpThreads, 3) state_passing_kernel(Plan p, Bu
   float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
   float aprod = 1.0f;
   constexpr int kBatch = kSeg < 8 ? kSeg : 8;  // loads issued together: only the FMA chain is serial
+  // warp-shuffle variant: lane layout and the decay windows of each step
+  constexpr int kGp = 32 / kSeg;  // float4 groups per warp pass
+  const int lane = threadIdx.x & 31, wbase = threadIdx.x & ~31;
+  const int kl = lane % kSeg, hl = lane / kSeg;
+  __shared__ float4 s_x4[kShfl ? kSpThreads : 1];  // per-thread aggregate, then prefix
+  if constexpr (kShfl) {
+    const float4* v4 = reinterpret_cast<const float4*>(s_buf);
+    const float a0 = kl < nk ? s_a[kl] : 1.0f;
+    for (int pass = 0; pass < 32 / kGp; ++pass) {
+      const int g = wbase + pass * kGp + hl;  // float4 group of this lane
+      float4 b = (kl < nk && e0 + g * 4 < p.PN) ? v4[kl * kSpThreads + g] : make_float4(0.f, 0.f, 0.f, 0.f);
+      float a = a0;
 #pragma unroll
-  for (int kb = 0; kb < kSeg; kb += kBatch) {
+      for (int d = 1; d < kSeg; d <<= 1) {
+        const float ao = __shfl_up_sync(0xffffffffu, a, d, kSeg);
+        const float4 bo = make_float4(__shfl_up_sync(0xffffffffu, b.x, d, kSeg), __shfl_up_sync(0xffffffffu, b.y, d, kSeg),
+                                      __shfl_up_sync(0xffffffffu, b.z, d, kSeg), __shfl_up_sync(0xffffffffu, b.w, d, kSeg));
+        if (kl >= d) {
+          b = fma4(a, bo, b);
+          a *= ao;
+        }
+      }
+      if (kl == nk - 1) {
+        s_x4[g] = b;
+        if (g == wbase) s_A[0] = a;  // the segment's decay product (every lane of chunk nk-1 agrees)
+      }
+    }
+    __syncthreads();
+    run = s_x4[threadIdx.x];
+    aprod = s_A[0];
+    __syncthreads();  // s_A is reused by the join
+  }
+#pragma unroll
+  for (int kb = 0; kb < (kShfl ? 0 : kSeg); kb += kBatch) {
     float4 x[kBatch];
 #pragma unroll
     for (int k = 0; k < kBatch; ++k)
@@ -238,8 +277,45 @@ __global__ void __launch_bounds__(kSpThreads, 3) state_passing_kernel(Plan p, Bu
   // 3) carry-in values of the segment's chunks, and the end of the chain
   float dp = 1.0f;  // product of the decays before chunk k (same order as aprod)
   float4 loc = make_float4(0.f, 0.f, 0.f, 0.f);  // the local scan again: value entering chunk k
+  if constexpr (kShfl) {
+    // the value entering chunk k: the exclusive scan (lane k-1's inclusive
+    // pair) applied to the segment's entering state
+    s_x4[threadIdx.x] = prefix;
+    __syncthreads();
+    const float4* v4 = reinterpret_cast<const float4*>(s_buf);
+    const float a0 = kl < nk ? s_a[kl] : 1.0f;
+    for (int pass = 0; pass < 32 / kGp; ++pass) {
+      const int g = wbase + pass * kGp + hl;
+      const bool gact = e0 + g * 4 < p.PN;
+      float4 b = (kl < nk && gact) ? v4[kl * kSpThreads + g] : make_float4(0.f, 0.f, 0.f, 0.f);
+      float a = a0;
 #pragma unroll
-  for (int kb = 0; kb < kSeg; kb += kBatch) {
+      for (int d = 1; d < kSeg; d <<= 1) {
+        const float ao = __shfl_up_sync(0xffffffffu, a, d, kSeg);
+        const float4 bo = make_float4(__shfl_up_sync(0xffffffffu, b.x, d, kSeg), __shfl_up_sync(0xffffffffu, b.y, d, kSeg),
+                                      __shfl_up_sync(0xffffffffu, b.z, d, kSeg), __shfl_up_sync(0xffffffffu, b.w, d, kSeg));
+        if (kl >= d) {
+          b = fma4(a, bo, b);
+          a *= ao;
+        }
+      }
+      float ae = __shfl_up_sync(0xffffffffu, a, 1, kSeg);
+      float4 be = make_float4(__shfl_up_sync(0xffffffffu, b.x, 1, kSeg), __shfl_up_sync(0xffffffffu, b.y, 1, kSeg),
+                              __shfl_up_sync(0xffffffffu, b.z, 1, kSeg), __shfl_up_sync(0xffffffffu, b.w, 1, kSeg));
+      if (kl == 0) {
+        ae = 1.0f;
+        be = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (kl < nk && gact) {
+        const size_t off = state_off(kl) + g * 4;
+        const float4 val = fma4(ae, s_x4[g], be);
+        store4(out + off, val);
+        if (kKeepF32) __stcs(reinterpret_cast<float4*>(f.S + off), val);
+      }
+    }
+  }
+#pragma unroll
+  for (int kb = 0; kb < (kShfl ? 0 : kSeg); kb += kBatch) {
    float4 x[kBatch];
 #pragma unroll
    for (int k2 = 0; k2 < kBatch; ++k2)
@@ -289,6 +365,8 @@ template <bool kBwd, bool kKeepF32, typename TOut>
 cudaError_t launch_sp(const Plan& p, const Bufs& f, cudaStream_t s) {
   const unsigned tiles = (unsigned)p.sp_chains * (kBwd ? p.sp_nseg_b : p.sp_nseg);
   auto kern = state_passing_kernel<kBwd, kKeepF32, TOut>;
+  if constexpr (!kBwd)
+    if (p.flags & SSD_SCAN_WARP_SHUFFLE) kern = state_passing_kernel<kBwd, kKeepF32, TOut, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)sp_smem_bytes<kBwd>());
   if (e != cudaSuccess) return e;

@@ -49,7 +49,7 @@ int make_plan(const ssd_problem* pr, Plan* p) {
   if (pr->dtype != SSD_F32 && pr->dtype != SSD_BF16) return SSD_ERR_INVALID_ARGUMENT;
   if (pr->flags & ~(SSD_HAS_INIT | SSD_HAS_SEQ_IDX | SSD_HAS_DFINAL | SSD_WANT_DINIT | SSD_KEEP_FWD_STATES |
                     SSD_TEST_DROP_SCAN_PUBLISH | SSD_PATH_MULTI_KERNEL | SSD_PATH_SINGLE_PASS |
-                    SSD_TEST_FEW_CTAS))
+                    SSD_TEST_FEW_CTAS | SSD_SCAN_WARP_SHUFFLE))
     return SSD_ERR_INVALID_ARGUMENT;
   if (pr->chunk_size > 256 || pr->chunk_size % 16 != 0) return SSD_ERR_UNSUPPORTED;
   if (!pow2_in(pr->headdim, 16, 128) || !pow2_in(pr->dstate, 16, 128)) return SSD_ERR_UNSUPPORTED;

@@ -113,6 +113,25 @@ def test_persistent_kernels_walk_several_units(name):
     assert_close(few, oracle_full(inp), inp.dtype)
 
 
+# the multi-kernel path's forward scan with its segments' local scans across
+# lanes (warp-shuffle Hillis-Steele steps) instead of inside each thread
+SHUFFLE_SCAN = ["bf16_many_segments", "fp32_many_segments", "bf16_chunk_aligned_resets",
+                "fp32_ragged_init_resets"]
+
+
+@pytest.mark.parametrize("name", SHUFFLE_SCAN)
+def test_warp_shuffle_scan_variant(name):
+    """SSD_SCAN_WARP_SHUFFLE: the same layer to rounding, against the oracle
+    and against the sequential in-thread scan on the same path."""
+    from mamba_selective_state_gb300 import _lib
+    inp = make_inputs(seed=7, **SMALL[name])
+    multi = _lib.SSD_PATH_MULTI_KERNEL
+    _, seq = run_device(inp, extra_flags=multi)
+    _, shf = run_device(inp, extra_flags=multi | _lib.SSD_SCAN_WARP_SHUFFLE)
+    assert_close(shf, oracle_full(inp), inp.dtype)
+    assert_close(shf, {k: v.numpy() for k, v in seq.items()}, inp.dtype)
+
+
 # bf16, headdim 64, d_state 64 or 128: the single-pass forward's shape set
 SINGLE_PASS = ["bf16_N128_G2", "bf16_N64_G4_varlen", "bf16_Q256_init", "bf16_single_token",
                "bf16_shorter_than_chunk", "bf16_Q32_mixed", "bf16_chunk_aligned_resets", "bf16_two_chunks",
