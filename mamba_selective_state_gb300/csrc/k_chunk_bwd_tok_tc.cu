@@ -38,7 +38,8 @@
 //     double-buffered pair, the dx stores;
 //   compute, per head: the M tile (units strictly below a row block's
 //     diagonal block use exp(l_i - l_r) exp(l_r - l_j) dt_j, l_r the block's
-//     first row, both exponentials <= 1, the second from a per-head table),
+//     first row, both exponentials <= 1, the second from a per-warp table
+//     of the warp's columns),
 //     then the epilogue of the previous head while the tensor core forms Z, W
 //     of this one.
 // Per-token results leave through fixed-order folds of the four warpgroups'
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(kThr, 1) chunk_bwd_tok_tc_kernel(Plan p, Bufs 
     }
     named_sync_compute();
 
-    // ---- M tile of head k (head hh of unit iu); then the factor table of head k+1
+    // ---- M tile of head k (head hh of unit iu)
     auto mask_pass = [&](int k, int iu, int hh) {
       const int us = iu % kRingU;
       const int* ut = utab + us * 8;
