@@ -65,6 +65,29 @@ def test_workspace_sizes(lib):
     assert lib.ssd_fwd_workspace_bytes(keep) == fw and lib.ssd_bwd_workspace_bytes(keep) == bw
 
 
+def header_flags():
+    """The problem-flag constants the header declares: name -> value."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = src[src.index("SSD_HAS_INIT"):]
+    body = body[:body.index("}")]
+    out = {}
+    for name, expr in re.findall(r"(SSD_\w+)\s*=\s*([^,\n]+)", body):
+        out[name] = eval(expr.replace("u", ""), {}, {})
+    return out
+
+
+def test_flag_constants_match_the_header_and_are_accepted(lib):
+    flags = header_flags()
+    assert {"SSD_KEEP_FWD_STATES", "SSD_TEST_FEW_CTAS", "SSD_SCAN_WARP_SHUFFLE"} <= set(flags)
+    for name, value in flags.items():
+        assert getattr(lib, name) == value, name
+        # every declared flag passes validation (the optional-input flags need
+        # their pointers at call time, not for the workspace query)
+        assert lib.ssd_fwd_workspace_bytes(prob(lib, flags=value)) > 0, name
+    unknown = 1 << (max(flags.values()).bit_length())
+    assert lib.ssd_fwd_workspace_bytes(prob(lib, flags=unknown)) == 0
+
+
 @pytest.mark.parametrize("bad", [
     dict(ngroups=3), dict(chunk_size=24), dict(chunk_size=512), dict(headdim=48),
     dict(dstate=256), dict(headdim=128, dstate=128), dict(seqlen=0), dict(batch=0),
