@@ -73,7 +73,8 @@ def kernel_model(cfg, dtype_bytes, keep=False):
     m["dt_cumsum"] = dict(bytes=T * H * s + 2 * per_tok, flops=0)
     m["chunk_state"] = dict(bytes=tokx + tokbc + 2 * per_tok + st32, flops=2 * units * Q * P * N)
     m["state_passing_fwd"] = dict(bytes=st32 + stS, flops=2 * units * P * N)
-    # the backward's forward pass also keeps the fp32 carry-in states (in place)
+    # a forward that keeps its intermediates, or the backward's recompute,
+    # also keeps the fp32 carry-in states (in place over the chunk states)
     m["state_passing_fwd_keep"] = dict(bytes=2 * st32 + stS, flops=2 * units * P * N)
     # chunk_scan: per (group, chunk) C B^T (at chunk 128 also C_rev B^T, the
     # copy with its row blocks reversed that balances the mask pass); per head
@@ -118,6 +119,10 @@ def kernel_model(cfg, dtype_bytes, keep=False):
                               flops=b * H * nq * fq)
     m["param_reduce"] = dict(bytes=b * nc * H * 4 * 4, flops=0)
     m["status_reset"] = dict(bytes=4, flops=0)
+    # a kept backward on the separate kernels zeroes the reverse scan's flags
+    # (one per (row, head, 512-element block, scan segment))
+    nflags = b * H * -(-(P * N) // 512) * max(-(-nc // 16), -(-nc // 8))
+    m["kept_scan_reset"] = dict(bytes=4 * nflags + 4, flops=0)
     # compulsory IO of the layer (fwd reads x dt B C, writes y; bwd reads x dt
     # B C dy, writes dx ddt dB dC)
     layer_io = (tokx + T * H * s + 2 * tokbc + tokx) + (2 * tokx + T * H * s + 2 * tokbc

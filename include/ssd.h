@@ -91,15 +91,20 @@ enum {
    * recompute -- dt_eff, the chunk-local cumsums of dt_eff * A, the per-chunk
    * decays and the carry-in state of every chunk (in the problem's dtype) --
    * and stamps the workspace with the problem's signature; ssd_fwd without it
-   * clears the stamp.  ssd_bwd with this flag, given that same workspace,
-   * takes them from there instead of recomputing them, where it runs its
-   * single-pass state chains (elsewhere it recomputes as usual and ignores
-   * the flag).  The inputs must be the ones that forward saw: the stamp
-   * covers the problem's shape, not its values.  A workspace without the
-   * stamp of this problem makes the backward report SSD_ERR_NO_KEPT_STATES
-   * in the device status word (its results are then garbage).  Forward
-   * results do not depend on the flag; backward results agree with the
-   * recomputing backward to rounding. */
+   * clears the stamp.  A forward on the separate kernels also keeps the fp32
+   * carry-in states (its scan writes them over the fp32 chunk states) and
+   * says so in the stamp.  ssd_bwd with this flag, given that same
+   * workspace, takes them from there instead of recomputing them: where it
+   * runs its single-pass state chains, from either forward; where it runs
+   * the separate kernels, from a forward on the separate kernels (if the
+   * same problem's forward takes the single-pass kernel, that backward
+   * recomputes as usual and ignores the flag).  The inputs must be the ones
+   * that forward saw: the stamp covers the problem's shape, not its values.
+   * A workspace without the stamp this backward needs makes it report
+   * SSD_ERR_NO_KEPT_STATES in the device status word (its results are then
+   * garbage).  Forward results do not depend on the flag; backward results
+   * agree with the recomputing backward to rounding (bit for bit on the
+   * separate kernels, which keep exactly what they would recompute). */
   SSD_KEEP_FWD_STATES = 16,
   /* Testing only: the first scan tile of the first state chain never
    * publishes its prefix, so the tiles after it exhaust their bounded wait

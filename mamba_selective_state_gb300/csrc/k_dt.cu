@@ -212,8 +212,19 @@ __global__ void __launch_bounds__(256) param_reduce_kernel(Plan p, Bufs f) {
 __global__ void status_reset_kernel(WsHeader* hdr, int mode, int sig, int sig_write) {
   int st = 0;
   if (mode == 1) hdr->kept_sig = sig_write;
-  if (mode == 2 && hdr->kept_sig != sig) st = kDevNoKept;
+  if (mode == 2 && (hdr->kept_sig & ~kKeptF32) != sig) st = kDevNoKept;
   hdr->status = st;
+}
+
+__global__ void __launch_bounds__(256) kept_scan_reset_kernel(Plan p, Bufs f) {
+  const long long nflags = (long long)p.sp_chains * p.sp_nslot;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nflags;
+       i += (long long)gridDim.x * blockDim.x)
+    f.flags_bwd[i] = 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    f.hdr->ticket_bwd = 0;
+    f.hdr->status = f.hdr->kept_sig == (p.kept_sig | kKeptF32) ? 0 : kDevNoKept;
+  }
 }
 
 }  // namespace
@@ -221,6 +232,15 @@ __global__ void status_reset_kernel(WsHeader* hdr, int mode, int sig, int sig_wr
 cudaError_t launch_status_reset(const Plan& p, const Bufs& f, cudaStream_t s) {
   set_kernel_name("status_reset");
   status_reset_kernel<<<1, 1, 0, s>>>(f.hdr, p.kept_mode, p.kept_sig, p.kept_sig_write);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kept_scan_reset(const Plan& p, const Bufs& f, cudaStream_t s) {
+  set_kernel_name("kept_scan_reset");
+  const long long nflags = (long long)p.sp_chains * p.sp_nslot;
+  const long long blocks = (nflags + 255) / 256;
+  const int grid = (int)(blocks < 1 ? 1 : (blocks > 1024 ? 1024 : blocks));
+  kept_scan_reset_kernel<<<grid, 256, 0, s>>>(p, f);
   return cudaGetLastError();
 }
 

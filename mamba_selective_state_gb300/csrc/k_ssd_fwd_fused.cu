@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(kThr, 1) ssd_fwd_fused_kernel(Plan p, Bufs f,
 }  // namespace
 
 bool ssd_fwd_fused_supported(const Plan& p) {
-  return p.dtype == SSD_BF16 && p.P == 64 && (p.N == 64 || p.N == 128);
+  return p.dtype == SSD_BF16 && p.P == 64 && p.Q == kQ && (p.N == 64 || p.N == 128);
 }
 
 cudaError_t launch_ssd_fwd_fused(const Plan& p, const Bufs& f, cudaStream_t s) {

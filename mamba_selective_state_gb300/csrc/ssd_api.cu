@@ -88,7 +88,8 @@ int make_plan(const ssd_problem* pr, Plan* p) {
                             (int64_t)(pr->flags & (SSD_HAS_INIT | SSD_HAS_SEQ_IDX))};
     for (int64_t k : keys)
       for (int byte = 0; byte < 8; ++byte) hsh = (hsh ^ (uint32_t)((k >> (8 * byte)) & 0xff)) * 16777619u;
-    p->kept_sig = (int)(hsh == 0 ? 1u : hsh);
+    hsh &= ~(uint32_t)kKeptF32;  // bit 0 tells which forward kept the intermediates
+    p->kept_sig = (int)(hsh == 0 ? 2u : hsh);
     p->kept_mode = 0;
     p->kept_sig_write = 0;
   }
@@ -248,11 +249,13 @@ int ssd_fwd(const ssd_problem* prob, const void* x, const void* dt, const float*
   bind_workspace(p, workspace, false, &f);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // every forward writes the kept-intermediates stamp: this problem's
-  // signature if it keeps them (both paths leave them in the workspace),
-  // else none
+  // signature if it keeps them (both paths leave them in the workspace; the
+  // separate kernels' scan also keeps the fp32 carry-in states), else none
+  const bool keep = (p.flags & SSD_KEEP_FWD_STATES) != 0;
+  const bool fused = use_fused_fwd(p);
   p.kept_mode = 1;
-  p.kept_sig_write = (p.flags & SSD_KEEP_FWD_STATES) ? p.kept_sig : 0;
-  if (use_fused_fwd(p)) {
+  p.kept_sig_write = keep ? (p.kept_sig | (fused ? 0 : kKeptF32)) : 0;
+  if (fused) {
     // no scan flags or tickets to reset, only the status word
     SSD_LAUNCH(launch_status_reset(p, f, s));
     SSD_LAUNCH(launch_ssd_fwd_fused(p, f, s));
@@ -260,7 +263,7 @@ int ssd_fwd(const ssd_problem* prob, const void* x, const void* dt, const float*
   }
   SSD_LAUNCH(launch_dt_cumsum(p, f, s));
   SSD_LAUNCH(launch_chunk_state(p, f, false, s));
-  SSD_LAUNCH(launch_state_passing(p, f, false, false, s));
+  SSD_LAUNCH(launch_state_passing(p, f, false, keep, s));
   SSD_LAUNCH(launch_chunk_scan(p, f, s));
   return SSD_OK;
 }
@@ -312,10 +315,17 @@ int ssd_bwd(const ssd_problem* prob, const void* x, const void* dt, const float*
     }
     SSD_LAUNCH(launch_state_chain(p, f, true, s));
   } else {
-    // recompute the forward intermediates: dt_eff, chunk cumsums, carry-in states
-    SSD_LAUNCH(launch_dt_cumsum(p, f, s));
-    SSD_LAUNCH(launch_chunk_state(p, f, false, s));
-    SSD_LAUNCH(launch_state_passing(p, f, false, true, s));
+    if ((p.flags & SSD_KEEP_FWD_STATES) && !use_fused_fwd(p)) {
+      // dt_eff, the chunk cumsums and decays and the carry-in states, bf16
+      // and fp32, are the separate-kernel forward's: check the stamp
+      p.kept_mode = 3;
+      SSD_LAUNCH(launch_kept_scan_reset(p, f, s));
+    } else {
+      // recompute the forward intermediates: dt_eff, chunk cumsums, carry-in states
+      SSD_LAUNCH(launch_dt_cumsum(p, f, s));
+      SSD_LAUNCH(launch_chunk_state(p, f, false, s));
+      SSD_LAUNCH(launch_state_passing(p, f, false, true, s));
+    }
     // gradient of the carry-in states from y, then the reverse state-passing scan
     SSD_LAUNCH(launch_chunk_state(p, f, true, s));
     SSD_LAUNCH(launch_state_passing(p, f, true, false, s));

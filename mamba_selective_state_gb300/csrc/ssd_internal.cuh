@@ -13,6 +13,12 @@ namespace ssd {
 // Status bits the kernels OR into the device status word.
 enum : int { kDevTimeout = 1, kDevNoKept = 2 };
 
+// Bit 0 of the kept-intermediates stamp: the forward that wrote it also kept
+// the fp32 carry-in states (the separate-kernel forward, whose scan writes
+// them over the chunk states).  The rest of the stamp is the problem's
+// signature, whose bit 0 is always clear.
+constexpr int kKeptF32 = 1;
+
 // State-passing scan tiling: one CTA scans kSpElems consecutive state elements
 // (kSpThreads threads x 4 floats) over a segment of consecutive chunks:
 // kSpSegF in the forward scan, kSpSegB in the reverse scan (which also stages
@@ -37,9 +43,11 @@ struct Plan {
   // dimensions
   int b, L, H, P, N, G, Q, nc, PN, hpg;  // hpg = heads per group
   int dtype, flags;
-  // nonzero signature of the problem's shape (the kept-intermediates stamp)
-  // and what the launch that resets the status word does with the stamp:
-  // 0 leave it, 1 write kept_sig_write, 2 check it against kept_sig
+  // nonzero signature of the problem's shape (the kept-intermediates stamp;
+  // bit 0 clear) and what the launch that resets the status word does with
+  // the stamp: 0 leave it, 1 write kept_sig_write, 2 check it against
+  // kept_sig whatever its kKeptF32 bit, 3 check it against kept_sig with
+  // the kKeptF32 bit set
   int kept_sig, kept_mode, kept_sig_write;
   long long Lp;                          // nc * Q (padded tokens per row)
   // state-passing scan tiling
@@ -141,6 +149,10 @@ __device__ __forceinline__ int seg_in_of(const Plan& p, const Bufs& f, int bi, i
 // Host launchers (each returns the launch's cudaError_t).
 cudaError_t launch_dt_cumsum(const Plan& p, const Bufs& f, cudaStream_t s);
 cudaError_t launch_status_reset(const Plan& p, const Bufs& f, cudaStream_t s);
+// The reset of a backward that runs the reverse scan without the forward's
+// recompute (which otherwise does it): zero the reverse scan's flags and
+// ticket, clear the status word and check the stamp (kept_mode 3).
+cudaError_t launch_kept_scan_reset(const Plan& p, const Bufs& f, cudaStream_t s);
 // backward: the reverse scan (dS, dinit, dL/da_c partials); keep_f32 (forward
 // only): also keep the fp32 carry-in states, in place over the chunk states.
 cudaError_t launch_state_passing(const Plan& p, const Bufs& f, bool backward, bool keep_f32, cudaStream_t s);

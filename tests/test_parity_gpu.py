@@ -201,13 +201,70 @@ def test_kept_forward_intermediates(name):
         assert float((kept[k] - rec[k]).abs().max()) <= 1e-2 * scale, k
 
 
-def test_kept_forward_intermediates_on_the_multi_kernel_path():
-    """Where the backward does not run the state chains it recomputes and
-    ignores the flag (its forward still stamps the workspace)."""
+# shapes of the separate kernels: CUDA-core fp32, tensor-core bf16 at d_state
+# 16 and 128, chunk 64 and 256, and a scan over many segments and checkpoints
+KEPT_MK = ["tiny_fp32", "fp32_ragged_init_resets", "bf16_N16_Q64", "bf16_N128_G2",
+           "bf16_many_segments", "bf16_Q256_init"]
+
+
+@pytest.mark.parametrize("name", KEPT_MK)
+def test_kept_forward_intermediates_on_the_multi_kernel_path(name):
+    """On the separate kernels the forward keeps dt_eff, the chunk cumsums
+    and decays and the carry-in states (bf16 and fp32; its scan writes the
+    fp32 ones over the chunk states), and the backward takes them instead of
+    recomputing: against the oracle, and bit for bit against the recomputing
+    backward, which runs the same deterministic kernels on the same inputs."""
     from mamba_selective_state_gb300 import _lib
-    inp = make_inputs(seed=13, **SMALL["bf16_N128_G2"])
-    _, got = run_device(inp, extra_flags=_lib.SSD_PATH_MULTI_KERNEL | _lib.SSD_KEEP_FWD_STATES)
-    assert_close(got, oracle_full(inp), inp.dtype)
+    mk = _lib.SSD_PATH_MULTI_KERNEL
+    inp = make_inputs(seed=13, **SMALL[name])
+    _, kept = run_device(inp, extra_flags=mk | _lib.SSD_KEEP_FWD_STATES)
+    assert_close(kept, oracle_full(inp), inp.dtype)
+    _, rec = run_device(inp, extra_flags=mk)
+    for k in kept:
+        assert torch.equal(kept[k], rec[k]), k
+
+
+def test_kept_multi_kernel_backward_runs_twice():
+    """Two backwards after one kept forward: the second finds the reverse
+    scan's flags and ticket reset (no forward recompute resets them there)
+    and gives the same bits."""
+    from mamba_selective_state_gb300 import _lib
+    inp = make_inputs(seed=15, **SMALL["bf16_many_segments"])
+    dev, a = run_device(inp, extra_flags=_lib.SSD_PATH_MULTI_KERNEL | _lib.SSD_KEEP_FWD_STATES)
+    for _ in range(2):
+        dev.bwd()
+        torch.cuda.synchronize()
+        assert dev.device_status() == 0
+        b = dev.results()
+        for k in a:
+            assert torch.equal(a[k], b[k]), k
+
+
+def test_kept_stamp_tells_which_forward_kept():
+    """The separate-kernel backward needs the fp32 carry-in states that only
+    the separate-kernel forward keeps: after a single-pass forward, or a
+    forward that keeps nothing, it reports SSD_ERR_NO_KEPT_STATES.  The
+    state-chain backward takes the intermediates of either forward."""
+    from mamba_selective_state_gb300 import _lib
+    from mamba_selective_state_gb300.runner import SSDDevice
+    keep, mk, sp = _lib.SSD_KEEP_FWD_STATES, _lib.SSD_PATH_MULTI_KERNEL, _lib.SSD_PATH_SINGLE_PASS
+    inp = make_inputs(seed=16, **SMALL["bf16_N128_G2"])
+    dev = SSDDevice(inp, device="cuda", extra_flags=mk | keep)
+    base_f, base_b = dev.fwd_prob.flags & ~(mk | keep), dev.bwd_prob.flags & ~(mk | keep)
+    for fwd_flags in (sp | keep, mk):
+        dev.fwd_prob.flags = base_f | fwd_flags
+        dev.fwd()
+        dev.bwd()
+        torch.cuda.synchronize()
+        assert dev.device_status() == _lib.SSD_ERR_NO_KEPT_STATES, fwd_flags
+    # separate-kernel forward, state-chain backward
+    dev.fwd_prob.flags = base_f | mk | keep
+    dev.bwd_prob.flags = base_b | sp | keep
+    dev.fwd()
+    dev.bwd()
+    torch.cuda.synchronize()
+    assert dev.device_status() == 0
+    assert_close(dev.results(), oracle_full(inp), inp.dtype)
 
 
 def test_missing_kept_intermediates_are_reported():
