@@ -138,10 +138,10 @@ def kernel_model(cfg, dtype_bytes, keep=False):
 # is the one captured, else null.
 NCU_TRAFFIC_WORKLOAD = "b2_L8192_bf16"
 NCU_TRAFFIC = {
-    "ssd_fwd_fused": (('k_ssd_fwd_fused.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.2920e+08, "4ddc8fb9d33d304d9556a00f82c613cbd1f0ac0f"),
-    "state_chain_bwd": (('k_state_chain.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.1255e+08, "48084b3c61770d52a92ca2cf77406050e6c31a2f"),
-    "chunk_bwd_tc": (('k_chunk_bwd_tok_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.4205e+08, "849f977ad997412af93ec2331ecfb20efe6b83ba"),
-    "chunk_bwd_dbc_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.9040e+08, "e6743280113ee360c2011c78b2c9ac37030f3a39"),
+    "ssd_fwd_fused": (('k_ssd_fwd_fused.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.2920e+08, "e7466ed302e73f4bef870b5dc3def204965de329"),
+    "state_chain_bwd": (('k_state_chain.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 4.1255e+08, "22731e6f826befc3796e68e18ad666a48df40a29"),
+    "chunk_bwd_tc": (('k_chunk_bwd_tok_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 7.4205e+08, "c2a97b3e80190f9c280635e1ce909908fa87c8b8"),
+    "chunk_bwd_dbc_tc": (('k_chunk_bwd_group_tc.cu', 'tc_common.cuh', 'ssd_internal.cuh'), 6.9040e+08, "fa041e274942dd2af296ed376774e190f5ad315a"),
 }
 
 
