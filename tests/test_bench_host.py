@@ -26,6 +26,10 @@ def test_kernel_model_counts_compulsory_bytes():
     assert m["state_passing_fwd"]["bytes"] == st32 + st32 // 2
     # reverse scan: dHloc and the fp32 carry-in states in, dS out
     assert m["state_passing_bwd"]["bytes"] == 2 * st32 + st32 // 2
+    # a kept backward on the separate kernels zeroes one scan flag per (row,
+    # head, 512-element state block, scan segment: 16 chunks forward, 8 in
+    # reverse) -- here 2 x 4 x 1 x 1 -- and writes the status word
+    assert m["kept_scan_reset"]["bytes"] == 4 * 8 + 4
     # the layer's own inputs and outputs, forward plus backward
     assert layer_io == (2 * tokx + T * 4 * 2 + 2 * tokbc) + (3 * tokx + 2 * T * 4 * 2 + 4 * tokbc)
 
